@@ -1,0 +1,218 @@
+/*
+ * flce.h -- C ABI of the GB300 (sm_103a) fused linear cross entropy library.
+ *
+ * Two operations:
+ *
+ *  flce_fwd_bwd  Fused linear cross entropy (FLCE): the lm_head projection
+ *                z = H W^T (+ b) fused with softmax cross entropy (ignore_index,
+ *                reduction none / sum / mean) and its backward (grad_hidden,
+ *                grad_weight, grad_bias), chunked over tokens so the [N, V]
+ *                logits never exist.  Defined by "Peak Performance, Minimized
+ *                Memory: Optimizing torchtune's performance with torch.compile
+ *                & Liger Kernel", section "Introduction to Liger Kernel",
+ *                Figure 1 "Fused Linear Cross Entropy" and its four steps
+ *                (flatten, project chunk by chunk, partial loss + chunk
+ *                logits gradient, hidden gradient + accumulated head
+ *                gradient); call shape from the liger-kernel 0.0.1 -> 0.1.1
+ *                PyPI diff, README "Compose Your Own Model" (weight, input,
+ *                target, then backward).
+ *
+ *  ce_fwd_bwd    Cross entropy on materialised logits [N, V]: loss and the
+ *                logits gradient in one call, the gradient optionally
+ *                written over the logits.  Defined by the same README,
+ *                "Kernels" list, CrossEntropy item (PyTorch CrossEntropyLoss
+ *                semantics, loss and gradient computed together, in-place
+ *                replacement of the input); logits dtypes and the reduction /
+ *                ignore contract from DeepSpeed PR #8540 (optional Liger
+ *                vocab-parallel CE backend), "Changes" and "Real-device
+ *                validation".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer to memory the caller owns.  The
+ *    library never allocates, frees or synchronises; all work is enqueued on
+ *    `stream` (a cudaStream_t; NULL is the legacy default stream) and runs
+ *    asynchronously.  Outputs are valid once the stream reaches the call.
+ *  - Matrices are row-major and contiguous.  bf16 is IEEE bfloat16; results
+ *    stored as bf16 are rounded to nearest even.
+ *  - Host-checkable faults (NULL required pointer, bad enum, bad shape or
+ *    alignment, workspace too small) return an error code BEFORE anything is
+ *    enqueued.  FLCE_ERR_CUDA means a launch failed (cudaGetLastError).
+ *  - Device-detected faults never trap.  They are OR-ed as bits into the
+ *    device status word: a target outside [0, V) that is not ignore_index sets
+ *    FLCE_STATUS_BIT_TARGET_RANGE and that row is treated as ignored; a
+ *    pipeline wait that exceeded its time limit sets FLCE_STATUS_BIT_TIMEOUT
+ *    and that call's outputs are undefined.  The status word is `status_dev`
+ *    when given (never cleared by the library), else the first 4 bytes of the
+ *    workspace (cleared at the start of each call).
+ *  - Calls that share a workspace must not overlap in time (same stream, or
+ *    ordered by events).
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared here so the header needs no CUDA. */
+typedef struct CUstream_st* flce_stream_t;
+
+typedef enum {
+  FLCE_REDUCTION_NONE = 0, /* per-row losses [N]                      */
+  FLCE_REDUCTION_SUM = 1,  /* sum over valid rows, scalar             */
+  FLCE_REDUCTION_MEAN = 2  /* sum / number of valid rows (NaN if 0)   */
+} flce_reduction_t;
+
+typedef enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 } flce_dtype_t;
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad enum       */
+  FLCE_ERR_UNSUPPORTED = 2,  /* dtype or layout not handled (e.g. H % 8)    */
+  FLCE_ERR_WORKSPACE = 3,    /* workspace NULL/too small/misaligned         */
+  FLCE_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed         */
+  FLCE_ERR_TARGET_RANGE = 5, /* value of a device status bit (see above)    */
+  FLCE_ERR_TIMEOUT = 6,      /* value of a device status bit (see above)    */
+  FLCE_ERR_MISALIGNED = 7    /* a pointer breaks its alignment requirement  */
+} flce_status_t;
+
+/* Bits of the device status word. */
+#define FLCE_STATUS_BIT_TARGET_RANGE 0x1
+#define FLCE_STATUS_BIT_TIMEOUT 0x2
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* flce_status_string(flce_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int flce_version(void);
+
+/* ------------------------------------------------------------------------
+ * Fused linear cross entropy
+ * ------------------------------------------------------------------------ */
+
+/* Token chunk used when flce_fwd_bwd is given chunk = 0, for these sizes. */
+int64_t flce_default_chunk(int64_t N, int64_t H, int64_t V);
+
+/* Bytes of workspace flce_fwd_bwd needs for these sizes (chunk 0 = default).
+ * It grows with chunk * V (the bf16 logits / grad-logits of one chunk) and
+ * with N (4 bytes of per-row loss), never with N * V.  Returns 0 for invalid
+ * sizes. */
+size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction);
+
+/*
+ * flce_fwd_bwd -- loss and gradients of cross_entropy(hidden @ weight^T + bias, target).
+ *
+ *  hidden        bf16 [N, H]; 16-byte aligned; H a multiple of 8 (TMA rows).
+ *  weight        bf16 [V, H]; 16-byte aligned.
+ *  bias          bf16 [V] or NULL (no bias).
+ *  target        int64 [N]; class ids in [0, V) or ignore_index.
+ *  N, H, V       tokens (>= 0), hidden size (>= 8, % 8 == 0), vocabulary (>= 1).
+ *  ignore_index  targets equal to it add no loss and no gradient (checked
+ *                before the range check, so it may lie inside [0, V)).
+ *  reduction     flce_reduction_t.  Mean divides by the number of valid
+ *                targets over all N rows.
+ *  chunk         tokens per chunk (>= 1), or 0 for flce_default_chunk.
+ *  grad_scale    upstream gradient g of the reduced loss; multiplies every
+ *                gradient (1.0 for plain loss.backward()).
+ *  grad_out_none fp32 [N] per-row upstream gradients, reduction NONE only
+ *                (gradient of sum_n g * grad_out[n] * loss_n); NULL = ones.
+ *  loss          fp32 output: [N] for NONE (0 for ignored rows), else [1].
+ *  grad_hidden   bf16 [N, H] output (always overwritten), or NULL to skip.
+ *  grad_weight   fp32 [V, H] output, 16-byte aligned, or NULL to skip.
+ *  grad_bias     fp32 [V] output, or NULL to skip (must be NULL if bias is).
+ *  accumulate    0: grad_weight / grad_bias are overwritten; 1: added to.
+ *  n_valid_out   int32 [1] output (number of valid targets), or NULL.
+ *  lse_out       fp32 [N] output: log-sum-exp of every row's logits, or NULL.
+ *  target_logit_out  fp32 [N] output: z[n, target_n] for valid rows, 0 for
+ *                ignored rows, or NULL.  (These two are the per-row partials
+ *                a vocabulary-parallel caller would combine across shards.)
+ *  workspace     device scratch of >= flce_workspace_size(...) bytes,
+ *                256-byte aligned; contents on entry are ignored.
+ *  status_dev    int32 device status word (see conventions), or NULL.
+ *  stream        CUDA stream.
+ *
+ * Arithmetic: the projection runs on the tensor cores (bf16 x bf16, fp32
+ * accumulation); the log-sum-exp and the target logit come from the fp32
+ * accumulator; the chunk's grad-logits are rounded to bf16 before the two
+ * backward products, which accumulate in fp32.
+ */
+flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* bias,
+                           const int64_t* target, int64_t N, int64_t H, int64_t V,
+                           int64_t ignore_index, int reduction, int64_t chunk,
+                           float grad_scale, const float* grad_out_none, float* loss,
+                           void* grad_hidden, float* grad_weight, float* grad_bias,
+                           int accumulate, int32_t* n_valid_out, float* lse_out,
+                           float* target_logit_out, void* workspace, size_t workspace_bytes,
+                           int32_t* status_dev, flce_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Cross entropy on materialised logits
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of workspace ce_fwd_bwd needs (per-row losses and counters). */
+size_t ce_workspace_size(int64_t N, int64_t V, int dtype, int reduction);
+
+/*
+ * ce_fwd_bwd -- loss and grad_logits of cross_entropy(logits, target).
+ *
+ *  logits        [N, V] of `dtype` (FLCE_DTYPE_BF16 or FLCE_DTYPE_FP32).
+ *  grad_logits   [N, V] of `dtype` output: scale_n * (softmax - onehot), 0 for
+ *                ignored rows.  May equal `logits` (in place: the logits are
+ *                consumed) or be a separate buffer (logits left unchanged),
+ *                or NULL (loss only).  Partial overlap is not allowed.
+ *  target        int64 [N].
+ *  ignore_index, reduction, grad_scale, grad_out_none, loss: as flce_fwd_bwd.
+ *  workspace     >= ce_workspace_size(...) bytes, 256-byte aligned.
+ *  status_dev, stream: as flce_fwd_bwd.
+ *
+ * Rows whose byte length is a multiple of 16 (V * sizeof(dtype)) with 16-byte
+ * aligned base pointers take the vectorised path; others the scalar path.
+ */
+flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const int64_t* target,
+                         int64_t N, int64_t V, int64_t ignore_index, int reduction,
+                         float grad_scale, const float* grad_out_none, float* loss,
+                         void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                         flce_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics (no counterpart on the pages)
+ * ------------------------------------------------------------------------ */
+
+/* Time limit of every pipeline wait inside the kernels, in nanoseconds of
+ * %globaltimer (default 2e9).  Applies to calls enqueued afterwards. */
+void flce_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/* Enqueues a kernel whose pipeline wait can never be satisfied: after
+ * timeout_ns it must give up, set FLCE_STATUS_BIT_TIMEOUT in *status_dev and
+ * return.  Checks the failure path of the bounded waits without faulting. */
+flce_status_t flce_selftest_wait_timeout(int32_t* status_dev, uint64_t timeout_ns,
+                                         flce_stream_t stream);
+
+/* Kernel timing: while enabled, every kernel the library enqueues is
+ * bracketed by a pair of CUDA events on its stream (the library creates up
+ * to `capacity` pairs once).  flce_profile_read synchronises on the recorded
+ * events and returns, for each recorded launch, its kernel id (below) and
+ * duration in ms; returns the number written (<= max).  Not thread-safe. */
+enum {
+  FLCE_KERNEL_COUNT_TARGETS = 0,
+  FLCE_KERNEL_GEMM_FWD = 1,
+  FLCE_KERNEL_ROW_FINALIZE = 2,
+  FLCE_KERNEL_GRAD_LOGITS = 3,
+  FLCE_KERNEL_GEMM_BWD = 4,
+  FLCE_KERNEL_LOSS_REDUCE = 5,
+  FLCE_KERNEL_CE_ROWS = 6,
+  FLCE_KERNEL_ZERO = 7
+};
+const char* flce_kernel_name(int kernel_id);
+flce_status_t flce_profile_enable(int capacity);
+void flce_profile_disable(void);
+int flce_profile_read(int* kernel_ids, float* ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLCE_H_ */

@@ -1,0 +1,436 @@
+// Host side of the C ABI declared in include/flce.h: argument validation,
+// workspace layout, TMA descriptor encoding and the launch sequence.  No
+// allocation and no synchronisation happen here; every kernel goes on the
+// caller's stream.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "flce_internal.h"
+
+namespace flce {
+
+int64_t ce_cta_capacity(int dtype, bool vector_path);
+int64_t ce_vector_elems(int dtype, bool vector_path);
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr size_t kAlign = 256;
+constexpr int64_t kDefaultChunkBudget = int64_t(1) << 30;  // bytes of bf16 chunk logits
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------- profiler
+struct Profiler {
+  bool enabled = false;
+  int capacity = 0;
+  int count = 0;
+  bool open = false;
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int> ids;
+} g_prof;
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] with row pitch `pitch_elems`, read in
+// 64 x 64 boxes with the 128-byte swizzle; out-of-range elements read as 0.
+bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t pitch_elems) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems * 2)};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- layouts
+struct FlceLayout {
+  int64_t chunk, num_chunks, vp, nvt;
+  size_t header, zbuf, partials, tgt_logit, row_lse, row_scale, row_tgt, loss_rows, total;
+};
+
+int64_t default_chunk(int64_t N, int64_t V) {
+  int64_t c = kDefaultChunkBudget / (V * 2);
+  c = c / 128 * 128;
+  if (c < 128) c = 128;
+  if (c > 16384) c = 16384;
+  if (N > 0 && c > N) c = N;
+  return c;
+}
+
+bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, FlceLayout* L) {
+  if (N < 0 || H < 8 || V < 1 || chunk < 0 || reduction < 0 || reduction > 2) return false;
+  if (N >= (int64_t(1) << 31) || V >= (int64_t(1) << 31) || H >= (int64_t(1) << 24)) return false;
+  L->chunk = chunk == 0 ? default_chunk(N, V) : chunk;
+  if (N > 0 && L->chunk > N) L->chunk = N;
+  if (L->chunk < 1) L->chunk = 1;
+  L->num_chunks = N > 0 ? ceil_div(N, L->chunk) : 0;
+  L->vp = round_up(static_cast<size_t>(V), 8);
+  L->nvt = ceil_div(V, kBN);
+  size_t off = 0;
+  L->header = off;
+  off = round_up(off + sizeof(WorkspaceHeader) + sizeof(unsigned int) * 2 * (L->num_chunks + 1), kAlign);
+  L->zbuf = off;
+  off = round_up(off + static_cast<size_t>(L->chunk) * L->vp * 2, kAlign);
+  L->partials = off;
+  off = round_up(off + static_cast<size_t>(L->chunk) * L->nvt * sizeof(float4), kAlign);
+  L->tgt_logit = off;
+  off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
+  L->row_lse = off;
+  off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
+  L->row_scale = off;
+  off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
+  L->row_tgt = off;
+  off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
+  L->loss_rows = off;
+  off = round_up(off + (reduction == FLCE_REDUCTION_NONE ? 0 : static_cast<size_t>(N) * 4), kAlign);
+  L->total = off;
+  return true;
+}
+
+struct CeLayout {
+  size_t header, loss_rows, total;
+};
+
+bool ce_layout(int64_t N, int64_t V, int dtype, int reduction, CeLayout* L) {
+  if (N < 0 || V < 1 || (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32) || reduction < 0 ||
+      reduction > 2)
+    return false;
+  L->header = 0;
+  L->loss_rows = round_up(sizeof(WorkspaceHeader) + 16, kAlign);
+  L->total = round_up(L->loss_rows + static_cast<size_t>(N) * 4, kAlign);
+  return true;
+}
+
+#define FLCE_TRY_CUDA(expr)                  \
+  do {                                       \
+    if ((expr) != cudaSuccess) return FLCE_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+void prof_begin(cudaStream_t s, int kernel_id) {
+  if (!g_prof.enabled || g_prof.count >= g_prof.capacity) return;
+  cudaEventRecord(g_prof.start[g_prof.count], s);
+  g_prof.ids[g_prof.count] = kernel_id;
+  g_prof.open = true;
+}
+
+void prof_end(cudaStream_t s) {
+  if (!g_prof.enabled || !g_prof.open) return;
+  cudaEventRecord(g_prof.stop[g_prof.count], s);
+  g_prof.count++;
+  g_prof.open = false;
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+const char* flce_status_string(flce_status_t s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG: bad argument (null pointer, size or enum)";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED: unsupported dtype or shape";
+    case FLCE_ERR_WORKSPACE: return "FLCE_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case FLCE_ERR_TARGET_RANGE: return "FLCE_ERR_TARGET_RANGE: a target outside [0, V) that is not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT: a pipeline wait exceeded its time limit";
+    case FLCE_ERR_MISALIGNED: return "FLCE_ERR_MISALIGNED: a pointer breaks its alignment requirement";
+  }
+  return "FLCE_UNKNOWN_STATUS";
+}
+
+int flce_version(void) { return kVersion; }
+
+int64_t flce_default_chunk(int64_t N, int64_t H, int64_t V) {
+  (void)H;
+  if (V < 1) return 0;
+  return default_chunk(N, V);
+}
+
+size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction) {
+  FlceLayout L;
+  if (!flce_layout(N, H, V, chunk, reduction, &L)) return 0;
+  return L.total;
+}
+
+flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* bias, const int64_t* target,
+                           int64_t N, int64_t H, int64_t V, int64_t ignore_index, int reduction,
+                           int64_t chunk, float grad_scale, const float* grad_out_none, float* loss,
+                           void* grad_hidden, float* grad_weight, float* grad_bias, int accumulate,
+                           int32_t* n_valid_out, float* lse_out, float* target_logit_out, void* workspace,
+                           size_t workspace_bytes, int32_t* status_dev, flce_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  FlceLayout L;
+  if (N < 0 || V < 1 || H < 1 || chunk < 0 || reduction < 0 || reduction > 2) return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!flce_layout(N, H, V, chunk, reduction, &L)) return FLCE_ERR_INVALID_ARG;
+  if (loss == nullptr || weight == nullptr) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (hidden == nullptr || target == nullptr)) return FLCE_ERR_INVALID_ARG;
+  if (grad_bias != nullptr && bias == nullptr) return FLCE_ERR_INVALID_ARG;
+  if (grad_out_none != nullptr && reduction != FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(bias, 16) || !aligned(grad_hidden, 16) ||
+      !aligned(grad_weight, 16) || !aligned(target, 8) || !aligned(loss, 4) || !aligned(grad_bias, 4))
+    return FLCE_ERR_MISALIGNED;
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < L.total) return FLCE_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
+  int* status = status_dev != nullptr ? status_dev : &hdr->status;
+  uint16_t* zbuf = reinterpret_cast<uint16_t*>(ws + L.zbuf);
+  float4* partials = reinterpret_cast<float4*>(ws + L.partials);
+  float* tgt_logit = reinterpret_cast<float*>(ws + L.tgt_logit);
+  float* row_lse = reinterpret_cast<float*>(ws + L.row_lse);
+  float* row_scale = reinterpret_cast<float*>(ws + L.row_scale);
+  int* row_tgt = reinterpret_cast<int*>(ws + L.row_tgt);
+  float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
+  const uint64_t timeout = g_timeout_ns.load();
+
+  const size_t hdr_bytes = sizeof(WorkspaceHeader) + sizeof(unsigned int) * 2 * (L.num_chunks + 1);
+  FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, hdr_bytes, stream));
+  FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, n_valid_out,
+                                     (grad_bias != nullptr && !accumulate) ? grad_bias : nullptr,
+                                     (grad_bias != nullptr && !accumulate) ? V : 0, stream));
+  if (N == 0) {
+    if (grad_weight != nullptr && !accumulate) FLCE_TRY_CUDA(launch_zero(grad_weight, V * H, stream));
+    if (reduction != FLCE_REDUCTION_NONE)
+      FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, 0, reduction, &hdr->n_valid, loss, stream, false));
+    return FLCE_OK;
+  }
+
+  CUtensorMap tm_h, tm_w, tm_z;
+  if (!make_map(&tm_h, hidden, H, N, H) || !make_map(&tm_w, weight, H, V, H)) return FLCE_ERR_CUDA;
+  const int sms = device_sm_count();
+  const bool want_grads = grad_hidden != nullptr || grad_weight != nullptr || grad_bias != nullptr;
+
+  for (int64_t k = 0; k < L.num_chunks; ++k) {
+    const int64_t row0 = k * L.chunk;
+    const int c_len = static_cast<int>(std::min<int64_t>(L.chunk, N - row0));
+    if (!make_map(&tm_z, zbuf, V, c_len, L.vp)) return FLCE_ERR_CUDA;
+
+    GemmParams g = {};
+    g.row0 = row0;
+    g.c_len = c_len;
+    g.H = static_cast<int>(H);
+    g.V = static_cast<int>(V);
+    g.f_num_m = static_cast<int>(ceil_div(c_len, kBM));
+    g.f_kblocks = static_cast<int>(ceil_div(H, kBK));
+    g.bias = static_cast<const uint16_t*>(bias);
+    g.target = target;
+    g.zbuf = zbuf;
+    g.ldz = L.vp;
+    g.partials = partials;
+    g.nvt = static_cast<int>(L.nvt);
+    g.tgt_logit = tgt_logit;
+    g.grad_hidden = static_cast<uint16_t*>(grad_hidden);
+    g.grad_weight = grad_weight;
+    g.gw_store = (k == 0 && !accumulate) ? 1 : 0;
+    g.status = status;
+    g.timeout_ns = timeout;
+
+    g.num_tiles = static_cast<int>(g.f_num_m * L.nvt);
+    g.tile_counter = &hdr->tile_counters[2 * k];
+    FLCE_TRY_CUDA(launch_gemm(kModeForward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+
+    RowParams r = {};
+    r.row0 = row0;
+    r.c_len = c_len;
+    r.N = N;
+    r.V = V;
+    r.ignore_index = ignore_index;
+    r.reduction = reduction;
+    r.grad_scale = grad_scale;
+    r.grad_out = grad_out_none;
+    r.target = target;
+    r.partials = partials;
+    r.nvt = static_cast<int>(L.nvt);
+    r.tgt_logit = tgt_logit;
+    r.n_valid = &hdr->n_valid;
+    r.row_lse = row_lse;
+    r.row_scale = row_scale;
+    r.row_tgt = row_tgt;
+    r.loss_rows = loss_rows;
+    r.lse_out = lse_out;
+    r.tl_out = target_logit_out;
+    r.status = status;
+    r.zbuf = zbuf;
+    r.ldz = L.vp;
+    r.grad_bias = grad_bias;
+    FLCE_TRY_CUDA(launch_row_finalize(r, stream));
+    if (!want_grads) continue;
+    FLCE_TRY_CUDA(launch_grad_logits(r, stream));
+
+    g.h_num_m = static_cast<int>(ceil_div(c_len, kBM));
+    g.h_kblocks = static_cast<int>(ceil_div(V, kBK));
+    g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, kBN)) : 0;
+    g.w_num_n = static_cast<int>(ceil_div(H, kBN));
+    g.w_kblocks = static_cast<int>(ceil_div(c_len, kBK));
+    const int w_tiles = grad_weight != nullptr ? static_cast<int>(ceil_div(V, kBM) * g.w_num_n) : 0;
+    g.num_tiles = g.h_tiles + w_tiles;
+    g.tile_counter = &hdr->tile_counters[2 * k + 1];
+    if (g.num_tiles > 0)
+      FLCE_TRY_CUDA(launch_gemm(kModeBackward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+  }
+  if (reduction != FLCE_REDUCTION_NONE)
+    FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, false));
+  return FLCE_OK;
+}
+
+size_t ce_workspace_size(int64_t N, int64_t V, int dtype, int reduction) {
+  CeLayout L;
+  if (!ce_layout(N, V, dtype, reduction, &L)) return 0;
+  return L.total;
+}
+
+flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const int64_t* target, int64_t N,
+                         int64_t V, int64_t ignore_index, int reduction, float grad_scale,
+                         const float* grad_out_none, float* loss, void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, flce_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
+  CeLayout L;
+  if (!ce_layout(N, V, dtype, reduction, &L)) return FLCE_ERR_INVALID_ARG;
+  if (loss == nullptr || (N > 0 && (logits == nullptr || target == nullptr))) return FLCE_ERR_INVALID_ARG;
+  if (grad_out_none != nullptr && reduction != FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 31) / 8) return FLCE_ERR_UNSUPPORTED;
+  const size_t esz = dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  if (!aligned(logits, esz) || !aligned(grad_logits, esz) || !aligned(target, 8) || !aligned(loss, 4))
+    return FLCE_ERR_MISALIGNED;
+  if (grad_logits != nullptr && grad_logits != logits) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(grad_logits);
+    const uintptr_t bytes = static_cast<uintptr_t>(N) * V * esz;
+    if (a < b + bytes && b < a + bytes) return FLCE_ERR_INVALID_ARG;  // partial overlap
+  }
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < L.total) return FLCE_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
+  int* status = status_dev != nullptr ? status_dev : &hdr->status;
+  float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
+
+  FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WorkspaceHeader) + 16, stream));
+  FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, stream));
+  if (N > 0) {
+    const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned(logits, 16) &&
+                     (grad_logits == nullptr || aligned(grad_logits, 16));
+    const int64_t cap = ce_cta_capacity(dtype, vec);
+    const int64_t epv = ce_vector_elems(dtype, vec);
+    int64_t cl = ceil_div(V, cap);
+    if (cl > 8) cl = 8;
+    if (cl < 1) cl = 1;
+    int64_t seg = ceil_div(V, cl);
+    seg = ceil_div(seg, epv) * epv;
+    cl = ceil_div(V, seg);
+    CeParams p = {};
+    p.logits = logits;
+    p.grad = grad_logits;
+    p.target = target;
+    p.N = N;
+    p.V = V;
+    p.ignore_index = ignore_index;
+    p.reduction = reduction;
+    p.grad_scale = grad_scale;
+    p.grad_out = grad_out_none;
+    p.loss_rows = loss_rows;
+    p.n_valid = &hdr->n_valid;
+    p.status = status;
+    p.cluster = static_cast<int>(cl);
+    p.seg_len = seg;
+    FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, true, stream));
+  }
+  if (reduction != FLCE_REDUCTION_NONE)
+    FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, N > 0));
+  return FLCE_OK;
+}
+
+void flce_set_wait_timeout_ns(uint64_t timeout_ns) {
+  g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1);
+}
+
+flce_status_t flce_selftest_wait_timeout(int32_t* status_dev, uint64_t timeout_ns, flce_stream_t stream) {
+  if (status_dev == nullptr || !aligned(status_dev, 4)) return FLCE_ERR_INVALID_ARG;
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FLCE_ERR_INVALID_ARG;
+  return launch_wait_selftest(status_dev, timeout_ns, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FLCE_OK
+             : FLCE_ERR_CUDA;
+}
+
+const char* flce_kernel_name(int id) {
+  switch (id) {
+    case FLCE_KERNEL_COUNT_TARGETS: return "count_targets";
+    case FLCE_KERNEL_GEMM_FWD: return "gemm_forward";
+    case FLCE_KERNEL_ROW_FINALIZE: return "row_finalize";
+    case FLCE_KERNEL_GRAD_LOGITS: return "grad_logits";
+    case FLCE_KERNEL_GEMM_BWD: return "gemm_backward";
+    case FLCE_KERNEL_LOSS_REDUCE: return "loss_reduce";
+    case FLCE_KERNEL_CE_ROWS: return "ce_rows";
+    case FLCE_KERNEL_ZERO: return "zero";
+  }
+  return "unknown";
+}
+
+flce_status_t flce_profile_enable(int capacity) {
+  if (capacity <= 0) return FLCE_ERR_INVALID_ARG;
+  if (static_cast<int>(g_prof.start.size()) < capacity) {
+    while (static_cast<int>(g_prof.start.size()) < capacity) {
+      cudaEvent_t a, b;
+      if (cudaEventCreate(&a) != cudaSuccess) return FLCE_ERR_CUDA;
+      if (cudaEventCreate(&b) != cudaSuccess) return FLCE_ERR_CUDA;
+      g_prof.start.push_back(a);
+      g_prof.stop.push_back(b);
+      g_prof.ids.push_back(-1);
+    }
+  }
+  g_prof.capacity = capacity;
+  g_prof.count = 0;
+  g_prof.open = false;
+  g_prof.enabled = true;
+  return FLCE_OK;
+}
+
+void flce_profile_disable(void) { g_prof.enabled = false; }
+
+int flce_profile_read(int* kernel_ids, float* ms, int max) {
+  int n = 0;
+  for (int i = 0; i < g_prof.count && n < max; ++i) {
+    float t = 0.f;
+    if (cudaEventSynchronize(g_prof.stop[i]) != cudaSuccess) break;
+    if (cudaEventElapsedTime(&t, g_prof.start[i], g_prof.stop[i]) != cudaSuccess) break;
+    kernel_ids[n] = g_prof.ids[i];
+    ms[n] = t;
+    ++n;
+  }
+  g_prof.count = 0;
+  return n;
+}
+
+}  // extern "C"

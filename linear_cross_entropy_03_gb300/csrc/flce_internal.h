@@ -1,0 +1,133 @@
+// Internal declarations shared by the kernels and the host layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/flce.h"
+
+namespace flce {
+
+// ---------------------------------------------------------------- GEMM tiles
+constexpr int kBM = 128;          // tile rows (tensor-memory lanes)
+constexpr int kBN = 256;          // tile columns (fp32 accumulator columns)
+constexpr int kBK = 64;           // k per pipeline stage (128 bytes of bf16)
+constexpr int kStages = 4;        // TMA -> MMA pipeline depth
+constexpr int kEpiWarps = 4;      // warps that drain the accumulators
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffering)
+constexpr int kTileRing = 8;      // scheduler ring of tile ids
+constexpr int kBoxBytes = 64 * 64 * 2;             // one TMA box: 64 x 64 bf16
+constexpr int kStageBytesA = kBM * kBK * 2;        // 16 KB
+constexpr int kStageBytesB = kBN * kBK * 2;        // 32 KB
+constexpr int kStageBytes = kStageBytesA + kStageBytesB;
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+
+enum GemmMode { kModeForward = 0, kModeBackward = 1 };
+
+struct GemmParams {
+  // chunk geometry
+  int64_t row0;      // first token of the chunk
+  int c_len;         // tokens in the chunk
+  int H, V;
+  int num_tiles;     // total tiles of the launch
+  // forward tiles: M = chunk tokens, N = vocabulary, K = H
+  int f_num_m, f_kblocks;
+  // backward tiles: grad_H (M = chunk tokens, N = H, K = V), then
+  // grad_W (M = vocabulary, N = H, K = chunk tokens)
+  int h_tiles, h_num_m, h_kblocks;
+  int w_num_n, w_kblocks;
+  // forward epilogue
+  const uint16_t* bias;     // bf16 [V] or null
+  const int64_t* target;    // [N]
+  uint16_t* zbuf;           // bf16 [c_len, ldz] chunk logits
+  int64_t ldz;
+  float4* partials;         // [c_len, nvt]: (max, sum exp(z - max), same over bf16(z), 0)
+  int nvt;
+  float* tgt_logit;         // [c_len]
+  // backward epilogue
+  uint16_t* grad_hidden;    // bf16 [N, H] or null
+  float* grad_weight;       // fp32 [V, H] or null
+  int gw_store;             // 1: overwrite grad_weight tiles, 0: add to them
+  // scheduling / failure
+  unsigned int* tile_counter;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+struct RowParams {
+  int64_t row0;
+  int c_len;
+  int64_t N, V;
+  int64_t ignore_index;
+  int reduction;
+  float grad_scale;
+  const float* grad_out;    // [N] or null
+  const int64_t* target;
+  const float4* partials;
+  int nvt;
+  const float* tgt_logit;
+  const int* n_valid;
+  float* row_lse;           // [c_len]: log-sum-exp of the bf16 logits (softmax of dZ)
+  float* row_scale;         // [c_len]
+  int* row_tgt;             // [c_len]: target or -1 when ignored
+  float* loss_rows;         // [N] (workspace, or the loss output for NONE)
+  float* lse_out;           // [N] or null
+  float* tl_out;            // [N] or null
+  int* status;
+  // grad-logits pass
+  uint16_t* zbuf;
+  int64_t ldz;
+  float* grad_bias;         // [V] or null
+};
+
+struct CeParams {
+  const void* logits;
+  void* grad;               // may alias logits, or null
+  const int64_t* target;
+  int64_t N, V;
+  int64_t ignore_index;
+  int reduction;
+  float grad_scale;
+  const float* grad_out;
+  float* loss_rows;         // [N]
+  const int* n_valid;
+  int* status;
+  int cluster;              // CTAs per row
+  int64_t seg_len;          // elements per CTA segment (multiple of the vector width)
+};
+
+// Header at the start of every workspace.
+struct WorkspaceHeader {
+  int status;
+  int n_valid;
+  int pad[2];
+  double loss_sum;
+  unsigned int tile_counters[];  // two per chunk
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
+                                 WorkspaceHeader* hdr, int num_counters, int clear_status,
+                                 int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
+                                 cudaStream_t s);
+cudaError_t launch_gemm(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,
+                        const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_row_finalize(const RowParams& p, cudaStream_t s);
+cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s);
+cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,
+                               float* loss, cudaStream_t s, bool pdl);
+cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
+cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool pdl, cudaStream_t s);
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+int gemm_max_smem_ok();  // sets kernel attributes once per device; 0 on failure
+int device_sm_count();
+
+// ---------------------------------------------------------------- profiler
+void prof_begin(cudaStream_t s, int kernel_id);
+void prof_end(cudaStream_t s);
+
+}  // namespace flce

@@ -1,0 +1,325 @@
+// Memory-bound row kernels of the fused linear cross entropy.
+//
+//  count_targets   number of valid targets over all N rows (the mean's
+//                  denominator, which must be known before any chunk's
+//                  gradient is formed) and the target range check.
+//  row_finalize    per chunk row: combine the per-vocabulary-tile (max, sum of
+//                  exp) partials into the log-sum-exp, the row loss and the
+//                  row's gradient scale.
+//  grad_logits     per chunk: dZ = scale * (softmax - onehot) written in place
+//                  over the chunk's bf16 logits, plus the bias gradient as
+//                  column sums (torchtune post "Peak Performance, Minimized
+//                  Memory ...", Figure 1, step 3; liger-kernel README
+//                  "Kernels", CrossEntropy item).
+//  loss_reduce     sum (or mean) of the per-row losses in a fixed order.
+#include <math.h>
+
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr int kCountThreads = 1024;
+
+__global__ void __launch_bounds__(kCountThreads)
+    count_targets_kernel(const int64_t* __restrict__ target, int64_t N, int64_t V, int64_t ignore_index,
+                         WorkspaceHeader* hdr, int* status, int32_t* n_valid_out, float* zero_a,
+                         int64_t zero_a_n) {
+  grid_dependents_launch();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_a_n; i += stride)
+    zero_a[i] = 0.f;
+  int cnt = 0;
+  bool bad = false;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
+    const int64_t t = target[i];
+    if (t != ignore_index) {
+      if (t >= 0 && t < V)
+        ++cnt;
+      else
+        bad = true;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, FLCE_STATUS_BIT_TARGET_RANGE);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  __shared__ int s_cnt[kCountThreads / 32];
+  __shared__ bool s_last;
+  if ((threadIdx.x & 31) == 0) s_cnt[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += s_cnt[w];
+    atomicAdd(&hdr->n_valid, total);
+    __threadfence();
+    const unsigned int ticket = atomicAdd(reinterpret_cast<unsigned int*>(&hdr->pad[0]), 1u);
+    s_last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last && threadIdx.x == 0 && n_valid_out != nullptr) {
+    __threadfence();
+    *n_valid_out = atomicAdd(&hdr->n_valid, 0);
+  }
+}
+
+constexpr int kFinalizeWarps = 8;
+
+__global__ void __launch_bounds__(32 * kFinalizeWarps) row_finalize_kernel(const RowParams p) {
+  grid_dependency_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kFinalizeWarps + warp;
+  if (r >= p.c_len) return;
+  const int64_t n = p.row0 + r;
+  const float4* pr = p.partials + static_cast<int64_t>(r) * p.nvt;
+  float m = -INFINITY;
+  for (int i = lane; i < p.nvt; i += 32) m = fmaxf(m, pr[i].x);
+  m = warp_max(m);
+  float s32 = 0.f, s16 = 0.f;
+  for (int i = lane; i < p.nvt; i += 32) {
+    const float4 q = pr[i];
+    const float e = __expf(q.x - m);
+    s32 += q.y * e;
+    s16 += q.z * e;
+  }
+  s32 = warp_sum(s32);
+  s16 = warp_sum(s16);
+  if (lane == 0) {
+    // The loss uses the log-sum-exp of the fp32 logits; the gradient's
+    // softmax is normalised over the bf16 logits it is formed from, so each
+    // dZ row sums to zero.
+    const float lse = m + logf(s32);
+    const float lse_bf16 = m + logf(s16);
+    const int64_t t = p.target[n];
+    const bool in_range = t >= 0 && t < p.V;
+    const bool valid = t != p.ignore_index && in_range;
+    if (t != p.ignore_index && !in_range) atomicOr(p.status, FLCE_STATUS_BIT_TARGET_RANGE);
+    const float zt = valid ? p.tgt_logit[r] : 0.f;
+    const float loss = valid ? lse - zt : 0.f;
+    float scale = 0.f;
+    if (valid) {
+      if (p.reduction == FLCE_REDUCTION_MEAN)
+        scale = p.grad_scale / static_cast<float>(*p.n_valid);
+      else if (p.reduction == FLCE_REDUCTION_SUM)
+        scale = p.grad_scale;
+      else
+        scale = p.grad_scale * (p.grad_out != nullptr ? p.grad_out[n] : 1.f);
+    }
+    p.row_lse[r] = lse_bf16;
+    p.row_scale[r] = scale;
+    p.row_tgt[r] = valid ? static_cast<int>(t) : -1;
+    p.loss_rows[n] = loss;
+    if (p.lse_out != nullptr) p.lse_out[n] = lse;
+    if (p.tl_out != nullptr) p.tl_out[n] = zt;
+  }
+}
+
+constexpr int kGlThreads = 256;
+constexpr int kGlCols = kGlThreads * 8;  // one 16-byte vector of bf16 per thread
+constexpr int kGlRows = 32;              // rows per block (bias column sums)
+constexpr int kGlUnroll = 4;
+
+__global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams p) {
+  __shared__ float s_lse[kGlRows], s_scale[kGlRows];
+  __shared__ int s_tgt[kGlRows];
+  grid_dependency_wait();
+  const int r0 = blockIdx.y * kGlRows;
+  const int rows = min(kGlRows, p.c_len - r0);
+  if (threadIdx.x < rows) {
+    s_lse[threadIdx.x] = p.row_lse[r0 + threadIdx.x];
+    s_scale[threadIdx.x] = p.row_scale[r0 + threadIdx.x];
+    s_tgt[threadIdx.x] = p.row_tgt[r0 + threadIdx.x];
+  }
+  __syncthreads();
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kGlCols + threadIdx.x * 8;
+  if (v0 >= p.V) return;
+  const int nval = p.V - v0 < 8 ? static_cast<int>(p.V - v0) : 8;
+  float cs[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cs[j] = 0.f;
+  uint16_t* base = p.zbuf + static_cast<int64_t>(r0) * p.ldz + v0;
+  for (int rr = 0; rr < rows; rr += kGlUnroll) {
+    uint4 in[kGlUnroll];
+#pragma unroll
+    for (int u = 0; u < kGlUnroll; ++u) {
+      if (rr + u < rows && s_tgt[rr + u] >= 0)
+        in[u] = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(rr + u) * p.ldz));
+      else
+        in[u] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kGlUnroll; ++u) {
+      const int r = rr + u;
+      if (r >= rows) break;
+      uint4* dst = reinterpret_cast<uint4*>(base + static_cast<int64_t>(r) * p.ldz);
+      const int t = s_tgt[r];
+      if (t < 0) {
+        __stcs(dst, make_uint4(0, 0, 0, 0));
+        continue;
+      }
+      const float lse = s_lse[r], sc = s_scale[r];
+      const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
+      float d[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        d[2 * i] = bf16_lo(w[i]);
+        d[2 * i + 1] = bf16_hi(w[i]);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float onehot = (v0 + j == t) ? 1.f : 0.f;
+        d[j] = sc * (__expf(d[j] - lse) - onehot);
+        if (j < nval) cs[j] += d[j];
+      }
+      uint4 o;
+      o.x = pack_bf16x2(d[0], d[1]);
+      o.y = pack_bf16x2(d[2], d[3]);
+      o.z = pack_bf16x2(d[4], d[5]);
+      o.w = pack_bf16x2(d[6], d[7]);
+      __stcs(dst, o);
+    }
+  }
+  if (p.grad_bias != nullptr) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nval) atomicAdd(p.grad_bias + v0 + j, cs[j]);
+  }
+}
+
+constexpr int kReduceThreads = 1024;
+
+__global__ void __launch_bounds__(kReduceThreads)
+    loss_reduce_kernel(const float* __restrict__ loss_rows, int64_t N, int reduction,
+                       const int* n_valid, float* loss) {
+  grid_dependency_wait();
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < N; i += kReduceThreads) acc += static_cast<double>(loss_rows[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  __shared__ double s_acc[kReduceThreads / 32];
+  if ((threadIdx.x & 31) == 0) s_acc[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double total = 0.0;
+    for (int w = 0; w < kReduceThreads / 32; ++w) total += s_acc[w];
+    if (reduction == FLCE_REDUCTION_MEAN) {
+      const int nv = *n_valid;
+      loss[0] = nv > 0 ? static_cast<float>(total / nv) : __int_as_float(0x7fc00000);
+    } else {
+      loss[0] = static_cast<float>(total);
+    }
+  }
+}
+
+__global__ void zero_kernel(float* p, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    p[i] = 0.f;
+}
+
+// One thread waits on a barrier nothing will ever arrive on.
+__global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_addr(&bar), 1);
+  fence_barrier_init();
+  const WaitCtl ctl{&abort_flag, status, timeout_ns};
+  if (mbar_wait(smem_addr(&bar), 0, ctl)) atomicOr(status, 0x100);  // cannot happen
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 132;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
+                                 WorkspaceHeader* hdr, int /*num_counters*/, int /*clear_status*/,
+                                 int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
+                                 cudaStream_t s) {
+  const int64_t work = N > zero_a_n ? N : zero_a_n;
+  int blocks = static_cast<int>((work + kCountThreads * 4 - 1) / (kCountThreads * 4));
+  blocks = blocks < 1 ? 1 : (blocks > sm_count() ? sm_count() : blocks);
+  prof_begin(s, FLCE_KERNEL_COUNT_TARGETS);
+  count_targets_kernel<<<blocks, kCountThreads, 0, s>>>(target, N, V, ignore_index, hdr, status,
+                                                       n_valid_out, zero_a, zero_a_n);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_row_finalize(const RowParams& p, cudaStream_t s) {
+  const int blocks = (p.c_len + kFinalizeWarps - 1) / kFinalizeWarps;
+  prof_begin(s, FLCE_KERNEL_ROW_FINALIZE);
+  RowParams pc = p;
+  void* args[] = {&pc};
+  const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(row_finalize_kernel), dim3(blocks),
+                                   dim3(32 * kFinalizeWarps), args, s, false);
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((p.V + kGlCols - 1) / kGlCols),
+                  static_cast<unsigned>((p.c_len + kGlRows - 1) / kGlRows));
+  prof_begin(s, FLCE_KERNEL_GRAD_LOGITS);
+  RowParams pc = p;
+  void* args[] = {&pc};
+  const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(grad_logits_kernel), grid,
+                                   dim3(kGlThreads), args, s, false);
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,
+                               float* loss, cudaStream_t s, bool pdl) {
+  prof_begin(s, FLCE_KERNEL_LOSS_REDUCE);
+  void* args[] = {&loss_rows, &N, &reduction, &n_valid, &loss};
+  const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(loss_reduce_kernel), dim3(1),
+                                   dim3(kReduceThreads), args, s, pdl);
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int blocks = static_cast<int>((n + 256 * 8 - 1) / (256 * 8));
+  blocks = blocks > 4 * sm_count() ? 4 * sm_count() : blocks;
+  prof_begin(s, FLCE_KERNEL_ZERO);
+  zero_kernel<<<blocks, 256, 0, s>>>(p, n);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+int device_sm_count() { return sm_count(); }
+
+}  // namespace flce

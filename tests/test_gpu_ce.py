@@ -1,0 +1,93 @@
+"""GPU parity of ce_fwd_bwd (cross entropy on materialised logits) against the
+fp64 oracle: bf16 and fp32 logits, in place and out of place, loss only,
+every reduction, vector and scalar row paths, register and streaming
+segments."""
+import numpy as np
+import pytest
+import torch
+
+import linear_cross_entropy_03_gb300 as flce
+import synthetic_inputs as si
+from oracle import flce_oracle as O
+from gpu_util import assert_grad, assert_loss, dev_bf16, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _logits_dev(logits, dtype):
+    if dtype == "bf16":
+        return dev_bf16(logits)
+    return torch.from_numpy(logits).cuda()
+
+
+def _run(logits, t, dtype, reduction, *, in_place=False, want_grad=True, grad_scale=1.0, grad_out=None):
+    z = _logits_dev(logits, dtype)
+    keep = z.clone()
+    go = torch.from_numpy(grad_out).cuda() if grad_out is not None else None
+    out = flce.cross_entropy(z, torch.from_numpy(t).cuda(), reduction=reduction, in_place=in_place,
+                             want_grad=want_grad, grad_scale=grad_scale, grad_out=go)
+    torch.cuda.synchronize()
+    if want_grad and not in_place:
+        assert torch.equal(z.view(torch.int16) if dtype == "bf16" else z,
+                           keep.view(torch.int16) if dtype == "bf16" else keep), "input logits changed"
+    loss = host(out["loss"])
+    grad = host(out["grad_logits"]) if want_grad else None
+    return loss, grad, int(out["status"].item())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("reduction", ["none", "sum", "mean"])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_ce_config_1024x32768(dtype, reduction, in_place):
+    c = si.CE_CONFIG
+    logits, t = si.make_ce_logits(c["n"], c["v"], c["seed"], std=c["std"], dtype=dtype,
+                                  ignore_frac=c["ignore_frac"])
+    go = si.make_grad_out(c["n"], 3) if reduction == "none" else None
+    ref = O.ce_reference(logits, t, reduction=reduction, grad_scale=0.7, grad_out=go)
+    loss, grad, status = _run(logits, t, dtype, reduction, in_place=in_place, grad_scale=0.7, grad_out=go)
+    assert status == 0
+    assert_loss(loss, ref["loss"], reduction)
+    assert_grad(grad, ref["dz"], "grad_logits")
+    assert np.all(grad[~ref["valid"]] == 0.0)
+    if reduction == "none":
+        assert np.all(loss[~ref["valid"]] == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("n,v", [(37, 1000), (64, 8192), (5, 8191), (9, 100003), (3, 1), (20, 70000),
+                                 (16, 262144)])
+def test_ce_shapes(dtype, n, v):
+    logits, t = si.make_ce_logits(n, v, 100 + n, std=2.0, dtype=dtype, ignore_frac=0.2)
+    ref = O.ce_reference(logits, t, reduction="mean")
+    loss, grad, status = _run(logits, t, dtype, "mean")
+    assert status == 0
+    assert_loss(loss, ref["loss"], "mean")
+    if ref["n_valid"] > 0 and v > 1:
+        assert_grad(grad, ref["dz"], "grad_logits")
+    assert np.all(grad[~ref["valid"]] == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_ce_loss_only(dtype):
+    logits, t = si.make_ce_logits(200, 5000, 4, dtype=dtype)
+    ref = O.ce_reference(logits, t, reduction="sum")
+    loss, _, status = _run(logits, t, dtype, "sum", want_grad=False)
+    assert status == 0
+    assert_loss(loss, ref["loss"], "sum")
+
+
+def test_ce_out_of_range_target():
+    logits, t = si.make_ce_logits(50, 300, 6)
+    t[4] = 300
+    ref = O.ce_reference(logits, t, reduction="mean")
+    loss, grad, status = _run(logits, t, "bf16", "mean")
+    assert status & 0x1
+    assert_loss(loss, ref["loss"], "mean")
+    assert np.all(grad[4] == 0.0)
+
+
+def test_ce_empty():
+    z = torch.empty(0, 100, dtype=torch.bfloat16, device="cuda")
+    out = flce.cross_entropy(z, torch.empty(0, dtype=torch.int64, device="cuda"), reduction="sum")
+    torch.cuda.synchronize()
+    assert out["loss"].item() == 0.0
