@@ -1,0 +1,466 @@
+"""Benchmark of the fused linear cross entropy hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * flce_fwd_bwd on the Llama-3-8B lm_head shape (N=16384 tokens, H=4096,
+    V=128256, bf16, 5% ignored targets, reduction mean, no bias): loss,
+    grad_hidden, fp32 grad_weight;
+  * ce_fwd_bwd on materialised bf16 logits [1024, 32768] ~ N(0, 2), in place.
+
+Printed as one JSON line (rank 0):
+  value      tokens/s of the step (all ranks), inputs resident in HBM, timed
+             with CUDA events on the launch stream;
+  e2e        the same metric through the C ABI with the step's inputs copied
+             from pinned host memory and the loss read back, every step;
+  roofline   the dominant kernel, its algorithmic FLOPs per launch over its
+             average launch time (CUDA events around each launch, recorded by
+             the library during the timed region) against the measured bf16
+             tensor peak;
+  ce_on_logits  GB/s of ce_fwd_bwd (one read + one write of the logits) with
+             L2 flushed between calls, against the measured HBM copy peak;
+  cpu_baseline  the fp64 oracle on a bounded sample of the same workload.
+
+`--impl reference` times the oracle itself as the reference arm.
+Multi-GPU (torchrun, one process per GPU): replicas only -- every rank runs
+the full workload on its own GPU; the only collectives are the barrier and
+the max-over-ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = dict(name="llama3_8b", n=16384, h=4096, v=128256, reduction="mean")
+CE_WORKLOAD = dict(n=1024, v=32768)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------- inputs
+def make_inputs(device):
+    import torch
+    import synthetic_inputs as si
+    w = WORKLOAD
+    inp = si.config_inputs(w["name"])
+    if w["n"] < inp.hidden.shape[0]:
+        inp = si.FlceInputs(inp.hidden[:w["n"]], inp.weight, inp.bias, inp.target[:w["n"]])
+    logits, ce_t = si.make_ce_logits(CE_WORKLOAD["n"], CE_WORKLOAD["v"], si.CE_CONFIG["seed"])
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    host = dict(hidden=bf16(inp.hidden), weight=bf16(inp.weight), target=torch.from_numpy(inp.target),
+                logits=bf16(logits), ce_target=torch.from_numpy(ce_t))
+    dev = {k: v.to(device) for k, v in host.items()}
+    return inp, host, dev
+
+
+class Step:
+    """Preallocated outputs and workspaces; one call = one step."""
+
+    def __init__(self, dev, device, chunk=0):
+        import torch
+        import linear_cross_entropy_03_gb300 as flce
+        self.flce = flce
+        w = WORKLOAD
+        self.n, self.h, self.v = w["n"], w["h"], w["v"]
+        self.red = flce.REDUCTIONS[w["reduction"]]
+        self.chunk = chunk if chunk else flce.flce_default_chunk(self.n, self.h, self.v)
+        self.dev = dev
+        self.loss = torch.empty(1, dtype=torch.float32, device=device)
+        self.grad_hidden = torch.empty(self.n, self.h, dtype=torch.bfloat16, device=device)
+        self.grad_weight = torch.empty(self.v, self.h, dtype=torch.float32, device=device)
+        self.ws_bytes = flce.flce_workspace_size(self.n, self.h, self.v, self.chunk, self.red)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
+        self.ce_loss = torch.empty(1, dtype=torch.float32, device=device)
+        self.ce_ws_bytes = flce.ce_workspace_size(cn, cv, "bf16", "mean")
+        self.ce_ws = torch.empty(self.ce_ws_bytes, dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.current_stream(device).cuda_stream
+
+    def flce_call(self):
+        d = self.dev
+        st = self.flce.flce_fwd_bwd(d["hidden"], d["weight"], None, d["target"], self.n, self.h, self.v,
+                                    -100, self.red, self.chunk, 1.0, None, self.loss, self.grad_hidden,
+                                    self.grad_weight, None, 0, None, None, None, self.ws, self.ws_bytes,
+                                    self.status, self.stream)
+        if st != 0:
+            raise RuntimeError(self.flce.flce_status_string(st))
+
+    def ce_call(self):
+        d = self.dev
+        cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
+        st = self.flce.ce_fwd_bwd(d["logits"], "bf16", d["logits"], d["ce_target"], cn, cv, -100, "mean", 1.0,
+                                  None, self.ce_loss, self.ce_ws, self.ce_ws_bytes, self.status, self.stream)
+        if st != 0:
+            raise RuntimeError(self.flce.flce_status_string(st))
+
+    def __call__(self):
+        self.flce_call()
+        self.ce_call()
+
+
+# --------------------------------------------------------------------- timing
+def timed_steps(step, steps, warmup, barrier):
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        step()
+    stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(stop)
+
+
+def kernel_profile(flce, records):
+    """{kernel name: (launches, total ms)} from the library's event records."""
+    agg = {}
+    for name, ms in records:
+        c, t = agg.get(name, (0, 0.0))
+        agg[name] = (c + 1, t + ms)
+    return agg
+
+
+def ce_bandwidth(step, iters=20):
+    """ce_fwd_bwd alone, L2 flushed (256 MB write) before every call."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=step.ws.device)
+    times = []
+    for i in range(iters + 3):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step.ce_call()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
+    alg_bytes = 2 * cn * cv * 2 + 12 * cn
+    ms = statistics.median(times)
+    return ms, alg_bytes
+
+
+def e2e_steps(step, host, dev, steps, warmup, barrier):
+    """Same step through the C ABI with host buffers: H2D copies of the inputs from
+    pinned memory and a D2H read of both losses, every step."""
+    import torch
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out = torch.empty(2, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out.numel() * out.element_size()
+
+    def one():
+        for k, v in pinned.items():
+            dev[k].copy_(v, non_blocking=True)
+        step()
+        out[0:1].copy_(step.loss, non_blocking=True)
+        out[1:2].copy_(step.ce_loss, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        one()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+# --------------------------------------------------------------------- oracle
+def oracle_sample(inp, rows: int):
+    """The fp64 oracle on the first `rows` tokens of the workload; returns seconds."""
+    from oracle import flce_oracle as O
+    t0 = time.perf_counter()
+    O.flce_reference(inp.hidden[:rows], inp.weight, None, inp.target[:rows],
+                     reduction=WORKLOAD["reduction"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, rows=512):
+    secs = oracle_sample(inp, rows)
+    return {"value": rows / secs, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, fwd+bwd of the first {rows} of {WORKLOAD['n']} tokens "
+                      f"(H={WORKLOAD['h']}, V={WORKLOAD['v']}, full grad_weight), {secs:.2f} s"}
+
+
+def workload_config(chunk=None):
+    w = WORKLOAD
+    cfg = {"workload": f"FLCE fwd+bwd, Llama-3-8B lm_head: N={w['n']} (batch 4 x seq 4096), H={w['h']}, "
+                       f"V={w['v']}, bf16 hidden/weight, fp32 grad_weight, 5% ignored, mean, no bias; "
+                       f"+ CE on bf16 logits [{CE_WORKLOAD['n']},{CE_WORKLOAD['v']}] in place",
+           "tokens_per_step": w["n"], "l2": "inputs larger than L2 (1.05 GB weight, 2.1 GB fp32 grad_weight)"}
+    if chunk is not None:
+        cfg["chunk"] = chunk
+    return cfg
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import synthetic_inputs as si
+    inp = si.config_inputs(WORKLOAD["name"])
+    rows = args.ref_rows
+    for _ in range(args.warmup_ref):
+        oracle_sample(inp, rows)
+    times = [oracle_sample(inp, rows) for _ in range(max(1, args.steps_ref))]
+    secs = statistics.mean(times)
+    value = rows / secs
+    line = {"impl": "reference", "metric": "FLCE fwd+bwd tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup_ref,
+            "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": workload_config(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                             "sample": f"fp64 numpy oracle on the first {rows} tokens per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--steps-ref", type=int, default=3)
+    ap.add_argument("--warmup-ref", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling runs only: use the first N tokens of the workload")
+    ap.add_argument("--only-flce", action="store_true", help="profiling runs only: skip the CE leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+        def barrier():
+            dist.barrier()
+    else:
+        def barrier():
+            pass
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import linear_cross_entropy_03_gb300 as flce
+
+    if args.tokens:
+        WORKLOAD["n"] = args.tokens
+    inp, host, dev = make_inputs(device)
+    step = Step(dev, device, args.chunk)
+    if args.only_flce:
+        step.ce_call = lambda: None
+    peaks, peak_src = load_peaks()
+
+    # launches per step, from one recorded step
+    flce.flce_profile_enable(4096)
+    step()
+    torch.cuda.synchronize()
+    per_step = flce.flce_profile_read(4096)
+    flce.flce_profile_disable()
+    launches_per_step = len(per_step)
+
+    # device-timed steps, kernel events recorded by the library meanwhile
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    flce.flce_profile_enable(launches_per_step * args.steps + 16)
+    clocks.start()
+    ms_total = timed_steps(step, args.steps, 0, barrier)
+    clock_info = clocks.stop()
+    records = flce.flce_profile_read(launches_per_step * args.steps + 16)
+    flce.flce_profile_disable()
+    status = int(step.status.item())
+
+    ms_step = ms_total / args.steps
+    t = torch.tensor([ms_step], device=device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item())
+    n, h, v = WORKLOAD["n"], WORKLOAD["h"], WORKLOAD["v"]
+    value = n * ws / (ms_step / 1e3)
+
+    prof = kernel_profile(flce, records)
+    total_k = sum(tk for _, tk in prof.values())
+    dom = max(prof, key=lambda k: prof[k][1])
+    chunk = step.chunk
+    n_chunks = math.ceil(n / chunk)
+
+    def gemm_flops(name):
+        per_chunk = 2.0 * chunk * h * v
+        return (2 * per_chunk) if name == "gemm_backward" else per_chunk
+
+    roof = None
+    if dom in ("gemm_backward", "gemm_forward"):
+        launches, tot_ms = prof[dom]
+        avg_ms = tot_ms / launches
+        achieved = gemm_flops(dom) / (avg_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "flops_per_launch": gemm_flops(dom), "avg_launch_ms": round(avg_ms, 4)}
+    step_flops = 6.0 * n * h * v
+    kernels = {k: {"launches": c, "ms_total": round(tk, 3), "share": round(tk / total_k, 4)}
+               for k, (c, tk) in sorted(prof.items(), key=lambda x: -x[1][1])}
+
+    ce_ms, ce_bytes = ce_bandwidth(step) if not args.only_flce else (float("nan"), 0)
+    ce_gbs = ce_bytes / (ce_ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        ms_e2e, h2d, d2h = e2e_steps(step, host, dev, max(3, args.steps // 2), 3, barrier)
+        ms_e2e /= max(3, args.steps // 2)
+        te = torch.tensor([ms_e2e], device=device)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": n * ws / (float(te.item()) / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(float(te.item()), 3)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.cpu_rows)
+
+    if rank == 0:
+        line = {
+            "metric": "FLCE fwd+bwd tokens/s (+ % bf16 tensor peak; CE GB/s vs HBM; peak scratch)",
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(chunk),
+            "tflops": round(step_flops / (ms_step / 1e3) / 1e12, 1),
+            "frac_of_bf16_peak": round(step_flops / (ms_step / 1e3) / 1e12 /
+                                       peaks.get("bf16_tflops_sustained", 1700.0), 4),
+            "roofline": roof,
+            "ce_on_logits": {"gbs": round(ce_gbs, 1), "ms": round(ce_ms, 4), "bytes": ce_bytes,
+                             "peak": peaks.get("hbm_gbs"), "frac": round(ce_gbs / peaks.get("hbm_gbs", 6800.0), 4),
+                             "l2": "flushed before every call"},
+            "scratch": {"workspace_bytes": step.ws_bytes, "full_logits_bytes": n * v * 2,
+                        "chunk": chunk, "chunks": n_chunks},
+            "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "kernels": kernels, "clocks": clock_info, "status": status, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
