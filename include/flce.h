@@ -179,6 +179,40 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
                          flce_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Cross entropy on logits without any caller-provided scratch
+ * ------------------------------------------------------------------------ */
+
+/* Largest N accepted by ce_fwd_bwd_noalloc. */
+#define FLCE_NOALLOC_MAX_ROWS 65536
+
+/*
+ * ce_fwd_bwd_noalloc -- the computation of ce_fwd_bwd for callers that cannot
+ * allocate device memory or hand over a workspace: for example a plugin whose
+ * enqueue step may not allocate, a process whose device memory belongs to
+ * another allocator, or a loop that cannot afford cudaMalloc's implicit
+ * synchronisation.  The pages have no counterpart; it is an integration aid.
+ *
+ * Its scratch (256 bytes plus 4 bytes per row) is a fixed device array inside
+ * the library, sized for FLCE_NOALLOC_MAX_ROWS rows (about 256 KiB, held by
+ * every GPU that loads the library until the process exits).  Arguments are
+ * those of ce_fwd_bwd without the workspace; N > FLCE_NOALLOC_MAX_ROWS returns
+ * FLCE_ERR_UNSUPPORTED before anything is enqueued.  Nothing is allocated or
+ * freed, by the library or by any routine it calls.
+ *
+ * The first call on a device looks the array's device address up (a one-time
+ * CUDA runtime query with that device current); make that first call before
+ * any stream capture.  All calls share the one array: calls that may overlap
+ * on the GPU (unordered streams) race and must be serialised by the caller.
+ * With status_dev NULL the status word is kept inside the array and cleared
+ * by each call.
+ */
+flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void* grad_logits,
+                                 const int64_t* target, int64_t N, int64_t V,
+                                 int64_t ignore_index, int reduction, float grad_scale,
+                                 const float* grad_out_none, float* loss, int32_t* status_dev,
+                                 flce_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics (no counterpart on the pages)
  * ------------------------------------------------------------------------ */
 

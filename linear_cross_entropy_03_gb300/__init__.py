@@ -17,7 +17,7 @@ from typing import Optional
 __all__ = [
     "REDUCTIONS", "DTYPES", "STATUS_BIT_TARGET_RANGE", "STATUS_BIT_TIMEOUT", "KERNEL_NAMES",
     "library_path", "lib", "flce_status_string", "flce_version", "flce_default_chunk",
-    "flce_workspace_size", "flce_fwd_bwd", "ce_workspace_size", "ce_fwd_bwd",
+    "flce_workspace_size", "flce_fwd_bwd", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
     "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
     "flce_profile_enable", "flce_profile_disable", "flce_profile_read",
     "fused_linear_cross_entropy", "cross_entropy", "FlceError",
@@ -48,6 +48,8 @@ _SIGNATURES = {
     "ce_workspace_size": (_SZ, [_I64, _I64, ctypes.c_int, ctypes.c_int]),
     "ce_fwd_bwd": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                   ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
+    "ce_fwd_bwd_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, ctypes.c_int,
+                                          ctypes.c_float, _P, _P, _P, _P]),
     "flce_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "flce_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_uint64, _P]),
     "flce_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -145,6 +147,20 @@ def ce_fwd_bwd(logits, dtype, grad_logits, target, N, V, ignore_index, reduction
         _ptr(logits), DTYPES[dtype] if isinstance(dtype, str) else int(dtype), _ptr(grad_logits),
         _ptr(target), N, V, ignore_index, _red(reduction), float(grad_scale), _ptr(grad_out_none),
         _ptr(loss), _ptr(workspace), int(workspace_bytes), _ptr(status_dev), _stream(stream))
+
+
+NOALLOC_MAX_ROWS = 65536
+
+
+def ce_fwd_bwd_noalloc(logits, dtype, grad_logits, target, N, V, ignore_index, reduction, grad_scale,
+                       grad_out_none, loss, status_dev, stream=None) -> int:
+    """ce_fwd_bwd without a workspace: the library's own fixed scratch array is
+    used, so nothing is allocated.  For callers that may not allocate device
+    memory; calls must not overlap on the GPU (they share that array)."""
+    return lib().ce_fwd_bwd_noalloc(
+        _ptr(logits), DTYPES[dtype] if isinstance(dtype, str) else int(dtype), _ptr(grad_logits),
+        _ptr(target), N, V, ignore_index, _red(reduction), float(grad_scale), _ptr(grad_out_none),
+        _ptr(loss), _ptr(status_dev), _stream(stream))
 
 
 def flce_set_wait_timeout_ns(ns: int) -> None:

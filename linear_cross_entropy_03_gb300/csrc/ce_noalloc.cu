@@ -1,0 +1,120 @@
+// ce_fwd_bwd_noalloc: cross entropy on logits for callers that must not
+// allocate device memory.
+//
+// Some callers cannot call cudaMalloc or hand the library a workspace of
+// their own: a plugin whose enqueue path is forbidden to allocate, a process
+// whose device memory is owned and accounted by another allocator, or a
+// latency-critical loop where cudaMalloc's implicit synchronisation and
+// unpredictable cost are not acceptable.  This entry point runs the same
+// kernels as ce_fwd_bwd, but its scratch (a small header and one fp32 loss
+// per row) lives in a file-scope device array that every GPU loading the
+// library holds until the process exits.  The caller passes only inputs and
+// outputs.
+//
+// The array is found with cudaGetSymbolAddress once per device, by the first
+// call made with that device current.  Every call shares the array: calls
+// that overlap on the GPU (different streams without ordering) race on it.
+#include <mutex>
+
+#include "flce_internal.h"
+
+namespace flce {
+int64_t ce_cta_capacity(int dtype, bool vector_path);
+int64_t ce_vector_elems(int dtype, bool vector_path);
+}  // namespace flce
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;  // WorkspaceHeader, rounded up
+constexpr size_t kScratchBytes = kHeaderBytes + sizeof(float) * FLCE_NOALLOC_MAX_ROWS;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+// Device address of the array for the current device (host code cannot use
+// the symbol itself as an address).
+void* scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+bool aligned_to(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+using namespace flce;
+
+extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void* grad_logits,
+                                            const int64_t* target, int64_t N, int64_t V,
+                                            int64_t ignore_index, int reduction, float grad_scale,
+                                            const float* grad_out_none, float* loss,
+                                            int32_t* status_dev, flce_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
+  if (N < 0 || V < 1 || reduction < 0 || reduction > 2) return FLCE_ERR_INVALID_ARG;
+  if (N > FLCE_NOALLOC_MAX_ROWS) return FLCE_ERR_UNSUPPORTED;  // beyond the static scratch
+  if (loss == nullptr || (N > 0 && (logits == nullptr || target == nullptr))) return FLCE_ERR_INVALID_ARG;
+  if (grad_out_none != nullptr && reduction != FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARG;
+  const size_t esz = dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  if (!aligned_to(logits, esz) || !aligned_to(grad_logits, esz) || !aligned_to(target, 8) ||
+      !aligned_to(loss, 4))
+    return FLCE_ERR_MISALIGNED;
+  if (grad_logits != nullptr && grad_logits != logits) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(grad_logits);
+    const uintptr_t bytes = static_cast<uintptr_t>(N) * V * esz;
+    if (a < b + bytes && b < a + bytes) return FLCE_ERR_INVALID_ARG;
+  }
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_address());
+  if (scratch == nullptr) return FLCE_ERR_CUDA;
+
+  WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(scratch);
+  int* status = status_dev != nullptr ? status_dev : &hdr->status;
+  float* loss_rows =
+      reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(scratch + kHeaderBytes);
+
+  // The header (valid-target count, block ticket, status) must start at zero.
+  if (cudaMemsetAsync(hdr, 0, kHeaderBytes, stream) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, stream) !=
+      cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (N > 0) {
+    const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned_to(logits, 16) &&
+                     (grad_logits == nullptr || aligned_to(grad_logits, 16));
+    const int64_t cap = ce_cta_capacity(dtype, vec);
+    const int64_t epv = ce_vector_elems(dtype, vec);
+    int64_t cl = ceil_div64(V, cap);
+    cl = cl > 8 ? 8 : (cl < 1 ? 1 : cl);
+    int64_t seg = ceil_div64(ceil_div64(V, cl), epv) * epv;
+    cl = ceil_div64(V, seg);
+    CeParams p = {};
+    p.logits = logits;
+    p.grad = grad_logits;
+    p.target = target;
+    p.N = N;
+    p.V = V;
+    p.ignore_index = ignore_index;
+    p.reduction = reduction;
+    p.grad_scale = grad_scale;
+    p.grad_out = grad_out_none;
+    p.loss_rows = loss_rows;
+    p.n_valid = &hdr->n_valid;
+    p.status = status;
+    p.cluster = static_cast<int>(cl);
+    p.seg_len = seg;
+    if (launch_ce_rows(p, dtype, vec, true, stream) != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  if (reduction != FLCE_REDUCTION_NONE &&
+      launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, N > 0) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return FLCE_OK;
+}
