@@ -214,23 +214,28 @@ def kernel_profile(flce, records):
 
 
 def ce_bandwidth(step, iters=20):
-    """ce_fwd_bwd alone, L2 flushed (256 MB write) before every call."""
+    """ce_fwd_bwd alone, L2 flushed (256 MB write) before every call.  Returns the
+    median time of the whole call and of its ce_rows kernel (library events)."""
     import torch
+    flce = step.flce
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=step.ws.device)
-    times = []
+    times, kernel = [], []
     for i in range(iters + 3):
         flush.fill_(i & 0xFF)
+        flce.flce_profile_enable(16)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step.ce_call()
         b.record()
         torch.cuda.synchronize()
+        rec = flce.flce_profile_read(16)
+        flce.flce_profile_disable()
         if i >= 3:
             times.append(a.elapsed_time(b))
+            kernel.append(sum(ms for name, ms in rec if name == "ce_rows"))
     cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
     alg_bytes = 2 * cn * cv * 2 + 12 * cn
-    ms = statistics.median(times)
-    return ms, alg_bytes
+    return statistics.median(times), statistics.median(kernel), alg_bytes
 
 
 def e2e_steps(step, host, dev, steps, warmup, barrier):
@@ -292,6 +297,10 @@ def workload_config(chunk=None):
     return cfg
 
 
+def variant_name(v):
+    return {1: "single-CTA 128x256 tiles", 2: "CTA-pair 256x256 tiles (cta_group::2)"}.get(v, str(v))
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -332,6 +341,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling runs only: use the first N tokens of the workload")
     ap.add_argument("--only-flce", action="store_true", help="profiling runs only: skip the CE leg")
+    ap.add_argument("--gemm-variant", type=int, default=0,
+                    help="tensor-core kernel form: 0 default, 1 one CTA per tile, 2 CTA pairs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -355,6 +366,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     import linear_cross_entropy_03_gb300 as flce
+    gemm_variant = flce.flce_set_gemm_variant(args.gemm_variant)
 
     if args.tokens:
         WORKLOAD["n"] = args.tokens
@@ -418,8 +430,9 @@ def main():
     kernels = {k: {"launches": c, "ms_total": round(tk, 3), "share": round(tk / total_k, 4)}
                for k, (c, tk) in sorted(prof.items(), key=lambda x: -x[1][1])}
 
-    ce_ms, ce_bytes = ce_bandwidth(step) if not args.only_flce else (float("nan"), 0)
+    ce_ms, ce_kernel_ms, ce_bytes = ce_bandwidth(step) if not args.only_flce else (float("nan"), float("nan"), 0)
     ce_gbs = ce_bytes / (ce_ms / 1e3) / 1e9
+    ce_kernel_gbs = ce_bytes / (ce_kernel_ms / 1e3) / 1e9 if ce_kernel_ms > 0 else float("nan")
 
     e2e = None
     if not args.no_e2e:
@@ -442,14 +455,18 @@ def main():
             "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(chunk),
+            "config": dict(workload_config(chunk), gemm=variant_name(gemm_variant)),
             "tflops": round(step_flops / (ms_step / 1e3) / 1e12, 1),
             "frac_of_bf16_peak": round(step_flops / (ms_step / 1e3) / 1e12 /
                                        peaks.get("bf16_tflops_sustained", 1700.0), 4),
             "roofline": roof,
             "ce_on_logits": {"gbs": round(ce_gbs, 1), "ms": round(ce_ms, 4), "bytes": ce_bytes,
                              "peak": peaks.get("hbm_gbs"), "frac": round(ce_gbs / peaks.get("hbm_gbs", 6800.0), 4),
-                             "l2": "flushed before every call"},
+                             "kernel": "ce_rows", "kernel_ms": round(ce_kernel_ms, 4),
+                             "kernel_gbs": round(ce_kernel_gbs, 1),
+                             "kernel_frac": round(ce_kernel_gbs / peaks.get("hbm_gbs", 6800.0), 4),
+                             "l2": "flushed before every call", "scope": "gbs/frac: whole ce_fwd_bwd call "
+                             "(count + ce_rows kernels); kernel_*: ce_rows alone"},
             "scratch": {"workspace_bytes": step.ws_bytes, "full_logits_bytes": n * v * 2,
                         "chunk": chunk, "chunks": n_chunks},
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

@@ -216,6 +216,14 @@ flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void* grad_logit
  * Diagnostics (no counterpart on the pages)
  * ------------------------------------------------------------------------ */
 
+/* Tensor-core kernel form used by flce_fwd_bwd calls enqueued afterwards:
+ * FLCE_GEMM_SINGLE_CTA (128 x 256 tiles, one CTA per tile) or
+ * FLCE_GEMM_CTA_PAIR (256 x 256 tiles on a pair of SMs, tcgen05 cta_group::2).
+ * 0 selects the default.  Returns the form now in effect. */
+#define FLCE_GEMM_SINGLE_CTA 1
+#define FLCE_GEMM_CTA_PAIR 2
+int flce_set_gemm_variant(int variant);
+
 /* Time limit of every pipeline wait inside the kernels, in nanoseconds of
  * %globaltimer (default 2e9).  Applies to calls enqueued afterwards. */
 void flce_set_wait_timeout_ns(uint64_t timeout_ns);

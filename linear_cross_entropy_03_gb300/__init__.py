@@ -18,7 +18,7 @@ __all__ = [
     "REDUCTIONS", "DTYPES", "STATUS_BIT_TARGET_RANGE", "STATUS_BIT_TIMEOUT", "KERNEL_NAMES",
     "library_path", "lib", "flce_status_string", "flce_version", "flce_default_chunk",
     "flce_workspace_size", "flce_fwd_bwd", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
-    "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
+    "flce_set_gemm_variant", "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
     "flce_profile_enable", "flce_profile_disable", "flce_profile_read",
     "fused_linear_cross_entropy", "cross_entropy", "FlceError",
 ]
@@ -50,6 +50,7 @@ _SIGNATURES = {
                                   ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
     "ce_fwd_bwd_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                           ctypes.c_float, _P, _P, _P, _P]),
+    "flce_set_gemm_variant": (ctypes.c_int, [ctypes.c_int]),
     "flce_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "flce_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_uint64, _P]),
     "flce_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -161,6 +162,16 @@ def ce_fwd_bwd_noalloc(logits, dtype, grad_logits, target, N, V, ignore_index, r
         _ptr(logits), DTYPES[dtype] if isinstance(dtype, str) else int(dtype), _ptr(grad_logits),
         _ptr(target), N, V, ignore_index, _red(reduction), float(grad_scale), _ptr(grad_out_none),
         _ptr(loss), _ptr(status_dev), _stream(stream))
+
+
+GEMM_SINGLE_CTA = 1
+GEMM_CTA_PAIR = 2
+
+
+def flce_set_gemm_variant(variant: int) -> int:
+    """Select the tensor-core kernel form (1: one CTA per 128x256 tile,
+    2: CTA pairs on 256x256 tiles, 0: default); returns the form in effect."""
+    return lib().flce_set_gemm_variant(int(variant))
 
 
 def flce_set_wait_timeout_ns(ns: int) -> None:

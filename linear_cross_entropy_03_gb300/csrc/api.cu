@@ -23,6 +23,7 @@ constexpr size_t kAlign = 256;
 constexpr int64_t kDefaultChunkBudget = int64_t(1) << 30;  // bytes of bf16 chunk logits
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_gemm_variant{FLCE_GEMM_SINGLE_CTA};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -257,9 +258,15 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
     g.status = status;
     g.timeout_ns = timeout;
 
+    const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
+    const int tile_m = pair ? 2 * kBM : kBM;
+    g.f_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.num_tiles = static_cast<int>(g.f_num_m * L.nvt);
     g.tile_counter = &hdr->tile_counters[2 * k];
-    FLCE_TRY_CUDA(launch_gemm(kModeForward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+    if (pair)
+      FLCE_TRY_CUDA(launch_gemm2(kModeForward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
+    else
+      FLCE_TRY_CUDA(launch_gemm(kModeForward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
 
     RowParams r = {};
     r.row0 = row0;
@@ -289,16 +296,20 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
     if (!want_grads) continue;
     FLCE_TRY_CUDA(launch_grad_logits(r, stream));
 
-    g.h_num_m = static_cast<int>(ceil_div(c_len, kBM));
+    g.h_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.h_kblocks = static_cast<int>(ceil_div(V, kBK));
     g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, kBN)) : 0;
     g.w_num_n = static_cast<int>(ceil_div(H, kBN));
     g.w_kblocks = static_cast<int>(ceil_div(c_len, kBK));
-    const int w_tiles = grad_weight != nullptr ? static_cast<int>(ceil_div(V, kBM) * g.w_num_n) : 0;
+    const int w_tiles = grad_weight != nullptr ? static_cast<int>(ceil_div(V, tile_m) * g.w_num_n) : 0;
     g.num_tiles = g.h_tiles + w_tiles;
     g.tile_counter = &hdr->tile_counters[2 * k + 1];
-    if (g.num_tiles > 0)
-      FLCE_TRY_CUDA(launch_gemm(kModeBackward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+    if (g.num_tiles > 0) {
+      if (pair)
+        FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
+      else
+        FLCE_TRY_CUDA(launch_gemm(kModeBackward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+    }
   }
   if (reduction != FLCE_REDUCTION_NONE)
     FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, false));
@@ -337,8 +348,13 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
   int* status = status_dev != nullptr ? status_dev : &hdr->status;
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
 
-  FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WorkspaceHeader) + 16, stream));
-  FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, stream));
+  if (N <= kCountSingleBlockMax) {
+    // one block zeroes the header and counts; the CE kernel overlaps it (PDL)
+    FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 1, status, nullptr, nullptr, 0, stream));
+  } else {
+    FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WorkspaceHeader) + 16, stream));
+    FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, stream));
+  }
   if (N > 0) {
     const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned(logits, 16) &&
                      (grad_logits == nullptr || aligned(grad_logits, 16));
@@ -365,11 +381,20 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
     p.status = status;
     p.cluster = static_cast<int>(cl);
     p.seg_len = seg;
+    p.loss_out = reduction != FLCE_REDUCTION_NONE ? loss : nullptr;  // fused final reduction
+    p.ticket = reinterpret_cast<unsigned int*>(&hdr->pad[1]);
     FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, true, stream));
+  } else if (reduction != FLCE_REDUCTION_NONE) {
+    FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, 0, reduction, &hdr->n_valid, loss, stream, false));
   }
-  if (reduction != FLCE_REDUCTION_NONE)
-    FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, N > 0));
   return FLCE_OK;
+}
+
+int flce_set_gemm_variant(int variant) {
+  if (variant == 0) variant = FLCE_GEMM_SINGLE_CTA;
+  if (variant != FLCE_GEMM_SINGLE_CTA && variant != FLCE_GEMM_CTA_PAIR) return g_gemm_variant.load();
+  g_gemm_variant.store(variant);
+  return variant;
 }
 
 void flce_set_wait_timeout_ns(uint64_t timeout_ns) {

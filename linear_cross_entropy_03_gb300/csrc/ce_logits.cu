@@ -6,11 +6,15 @@
 //
 // HBM-bound design: each row is split into `cluster` contiguous segments,
 // one CTA per segment, the CTAs of a row forming a thread-block cluster.  A
-// CTA holds its segment in registers (four 16-byte vectors per thread,
-// coalesced across the CTA), reduces (max, sum of exp) with warp shuffles,
-// and the cluster combines the segments' partials through distributed shared
-// memory.  The gradient is then formed from the registers and written once,
-// so every logit is read once and written once.  Segments longer than the
+// CTA holds its segment in registers (16-byte vectors, coalesced across the
+// CTA), reduces (max, sum of exp) with warp shuffles, and every warp combines
+// the row's segment partials straight from the other CTAs' shared memory
+// (distributed shared memory).  The gradient is then formed from the
+// registers and written once, so every logit is read once and written once.
+// The cluster barrier is split: the arrive that says "done reading the other
+// CTAs' partials" is issued before the gradient pass and its wait only at
+// exit.  For sum / mean the last CTA to finish adds the row losses in a fixed
+// order (deterministic) and writes the result.  Segments longer than the
 // register capacity fall back to a two-read streaming loop.
 #include <cooperative_groups.h>
 #include <math.h>
@@ -44,7 +48,7 @@ __device__ __forceinline__ uint16_t from_f<uint16_t>(float v) {
   return static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
 }
 
-// A packet of EPV consecutive elements (EPV * sizeof(T) == 16 for the vector path).
+// EPV consecutive elements (EPV * sizeof(T) == 16 on the vector path).
 template <typename T, int EPV>
 struct Packet {
   T v[EPV];
@@ -71,39 +75,55 @@ __device__ __forceinline__ void store_packet(T* dst, const Packet<T, EPV>& pk) {
   }
 }
 
-__device__ __forceinline__ float block_max(float v, float* red) {
-  v = warp_max(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < kCeWarps; ++w) r = fmaxf(r, red[w]);
-  return r;
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  v = warp_sum(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = 0.f;
+// Gradient of one packet, written back into the packet; returns the target
+// logit if the packet holds the target (else leaves zt unchanged).
+template <typename T, int EPV>
+__device__ __forceinline__ void grad_packet(Packet<T, EPV>& pk, int64_t e, int64_t t, bool valid, float scale,
+                                            float lse, float& zt, bool& found) {
 #pragma unroll
-  for (int w = 0; w < kCeWarps; ++w) r += red[w];
-  return r;
+  for (int k = 0; k < EPV; ++k) {
+    const float z = to_f<T>(pk.v[k]);
+    const bool hit = valid && (e + k == t);
+    if (hit) {
+      zt = z;
+      found = true;
+    }
+    const float d = valid ? scale * (__expf(z - lse) - (hit ? 1.f : 0.f)) : 0.f;
+    pk.v[k] = from_f<T>(d);
+  }
+}
+
+template <typename T, int EPV>
+__device__ __forceinline__ void find_target(const Packet<T, EPV>& pk, int64_t e, int64_t t, float& zt,
+                                            bool& found) {
+#pragma unroll
+  for (int k = 0; k < EPV; ++k)
+    if (e + k == t) {
+      zt = to_f<T>(pk.v[k]);
+      found = true;
+    }
 }
 
 template <typename T, int EPV>
 __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
-  __shared__ float red[kCeWarps];
-  __shared__ float2 part;     // this CTA's (max, sum of exp), read by the cluster
-  __shared__ float lse_bcast;
+  __shared__ float s_max[kCeWarps], s_sum[kCeWarps];
+  __shared__ float2 part;  // this CTA's (max, sum of exp), read by the whole cluster
+  __shared__ int s_last;
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int seg = static_cast<int>(cluster.block_rank());
-  const int64_t row = blockIdx.x / p.cluster;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cl = p.cluster;
+  const int seg = cl > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+  const int64_t row = blockIdx.x / cl;
   const int64_t seg_start = seg * p.seg_len;
   const int64_t seg_end = min(p.V, seg_start + p.seg_len);
   const T* x = static_cast<const T*>(p.logits) + row * p.V;
@@ -126,16 +146,6 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
       for (int k = 0; k < EPV; ++k)
         if (e + k < seg_end) m_thr = fmaxf(m_thr, to_f<T>(buf[i].v[k]));
     }
-    const float m_cta = block_max(m_thr, red);
-#pragma unroll
-    for (int i = 0; i < kCeVecs; ++i) {
-      const int64_t e = seg_start + static_cast<int64_t>(i * kCeThreads + threadIdx.x) * EPV;
-#pragma unroll
-      for (int k = 0; k < EPV; ++k)
-        if (e + k < seg_end) s_thr += __expf(to_f<T>(buf[i].v[k]) - m_cta);
-    }
-    const float s_cta = block_sum(s_thr, red);
-    if (threadIdx.x == 0) part = make_float2(m_cta, s_cta);
   } else {
     // streaming pass 1: online (max, sum of exp) per thread
     for (int64_t b = seg_start; b < seg_end; b += kCap) {
@@ -160,29 +170,61 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
         }
       }
     }
-    const float m_cta = block_max(m_thr, red);
-    const float s_cta = block_sum(m_thr > -INFINITY ? s_thr * __expf(m_thr - m_cta) : 0.f, red);
-    if (threadIdx.x == 0) part = make_float2(m_cta, s_cta);
   }
 
-  // combine the row's segments across the cluster
-  cluster.sync();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int r = 0; r < p.cluster; ++r) M = fmaxf(M, cluster.map_shared_rank(&part, r)->x);
-    float S = 0.f;
-    for (int r = 0; r < p.cluster; ++r) {
-      const float2 q = *cluster.map_shared_rank(&part, r);
-      if (q.x > -INFINITY) S += q.y * __expf(q.x - M);
-    }
-    lse_bcast = M + logf(S);
+  // CTA max
+  {
+    const float wm = warp_max(m_thr);
+    if (lane == 0) s_max[warp] = wm;
   }
-  cluster.sync();  // also keeps every CTA's `part` alive until all have read it
-  const float lse = lse_bcast;
+  __syncthreads();
+  float m_cta = s_max[0];
+#pragma unroll
+  for (int w = 1; w < kCeWarps; ++w) m_cta = fmaxf(m_cta, s_max[w]);
+
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < kCeVecs; ++i) {
+      const int64_t e = seg_start + static_cast<int64_t>(i * kCeThreads + threadIdx.x) * EPV;
+#pragma unroll
+      for (int k = 0; k < EPV; ++k)
+        if (e + k < seg_end) s_thr += __expf(to_f<T>(buf[i].v[k]) - m_cta);
+    }
+  } else {
+    s_thr = m_thr > -INFINITY ? s_thr * __expf(m_thr - m_cta) : 0.f;
+  }
+  {
+    const float ws = warp_sum(s_thr);
+    if (lane == 0) s_sum[warp] = ws;
+  }
+  __syncthreads();
+
+  float lse;
+  if (cl > 1) {
+    if (threadIdx.x == 0) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCeWarps; ++w) s += s_sum[w];
+      part = make_float2(m_cta, s);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    float2 q = make_float2(-INFINITY, 0.f);
+    if (lane < cl) q = *cg::this_cluster().map_shared_rank(&part, lane);
+    const float M = warp_max(q.x);
+    const float S = warp_sum(q.x > -INFINITY ? q.y * __expf(q.x - M) : 0.f);
+    lse = M + logf(S);
+    cluster_arrive_relaxed();  // done with the other CTAs' shared memory
+  } else {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCeWarps; ++w) s += s_sum[w];
+    lse = m_cta + logf(s);
+  }
 
   const int64_t t = p.target[row];
   const bool valid = t != p.ignore_index && t >= 0 && t < p.V;
-  grid_dependency_wait();  // n_valid comes from the preceding count kernel
+  grid_dependency_wait();  // n_valid (and the zeroed ticket) come from the preceding count kernel
   float scale = 0.f;
   if (valid) {
     if (p.reduction == FLCE_REDUCTION_MEAN)
@@ -192,31 +234,24 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
     else
       scale = p.grad_scale * (p.grad_out != nullptr ? p.grad_out[row] : 1.f);
   }
-  if (!valid && seg == 0 && threadIdx.x == 0) p.loss_rows[row] = 0.f;
 
-  auto emit = [&](Packet<T, EPV>& pk, int64_t e) {
-#pragma unroll
-    for (int k = 0; k < EPV; ++k) {
-      const float z = to_f<T>(pk.v[k]);
-      if (valid && e + k == t) p.loss_rows[row] = lse - z;
-      const float d = valid ? scale * (__expf(z - lse) - (e + k == t ? 1.f : 0.f)) : 0.f;
-      pk.v[k] = from_f<T>(d);
-    }
-  };
-
+  float zt = 0.f;
+  bool found = false;  // this thread holds the target logit
   if (in_regs) {
 #pragma unroll
     for (int i = 0; i < kCeVecs; ++i) {
       const int64_t e = seg_start + static_cast<int64_t>(i * kCeThreads + threadIdx.x) * EPV;
       if (e < seg_end) {
         if (g == nullptr) {
-          if (valid && t >= e && t < e + EPV) p.loss_rows[row] = lse - to_f<T>(buf[i].v[t - e]);
+          find_target<T, EPV>(buf[i], e, valid ? t : -1, zt, found);
         } else {
-          emit(buf[i], e);
+          grad_packet<T, EPV>(buf[i], e, t, valid, scale, lse, zt, found);
           if (e + EPV <= seg_end) {
             store_packet<T, EPV>(g + e, buf[i]);
           } else {
-            for (int k = 0; k < EPV && e + k < seg_end; ++k) g[e + k] = buf[i].v[k];
+#pragma unroll
+            for (int k = 0; k < EPV; ++k)
+              if (e + k < seg_end) g[e + k] = buf[i].v[k];
           }
         }
       }
@@ -230,19 +265,259 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
           Packet<T, EPV> pk;
           load_packet<T, EPV>(pk, x + e);
           if (g == nullptr) {
-            if (valid && t >= e && t < e + EPV && t < seg_end) p.loss_rows[row] = lse - to_f<T>(pk.v[t - e]);
+            find_target<T, EPV>(pk, e, valid ? t : -1, zt, found);
           } else {
-            emit(pk, e);
+            grad_packet<T, EPV>(pk, e, t, valid, scale, lse, zt, found);
             if (e + EPV <= seg_end) {
               store_packet<T, EPV>(g + e, pk);
             } else {
-              for (int k = 0; k < EPV && e + k < seg_end; ++k) g[e + k] = pk.v[k];
+#pragma unroll
+              for (int k = 0; k < EPV; ++k)
+                if (e + k < seg_end) g[e + k] = pk.v[k];
             }
           }
         }
       }
     }
   }
+  if (found) p.loss_rows[row] = lse - zt;
+  if (!valid && seg == 0 && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+
+  if (p.loss_out != nullptr) {
+    // sum / mean: the last CTA to finish adds the row losses in a fixed order
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned int ticket = atomicAdd(p.ticket, 1u);
+      s_last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      double acc = 0.0;
+      for (int64_t i = threadIdx.x; i < p.N; i += kCeThreads) acc += static_cast<double>(__ldcg(p.loss_rows + i));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      __shared__ double s_acc[kCeWarps];
+      if (lane == 0) s_acc[warp] = acc;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double total = 0.0;
+#pragma unroll
+        for (int w = 0; w < kCeWarps; ++w) total += s_acc[w];
+        if (p.reduction == FLCE_REDUCTION_MEAN) {
+          const int nv = *p.n_valid;
+          p.loss_out[0] = nv > 0 ? static_cast<float>(total / nv) : __int_as_float(0x7fc00000);
+        } else {
+          p.loss_out[0] = static_cast<float>(total);
+        }
+      }
+    }
+  }
+  if (cl > 1) cluster_wait_acquire();  // the other CTAs have finished reading `part`
+}
+
+// ---------------------------------------------------------------------------
+// Row-ring form, for rows that fit in shared memory (V * sizeof(T) <= 72 KB,
+// 16-byte aligned rows): one persistent 512-thread CTA per SM takes rows
+// blockIdx.x, blockIdx.x + gridDim.x, ...; one thread keeps `depth` whole-row
+// TMA bulk loads in flight in a shared-memory ring, so the SM streams without
+// pause.  Each row is copied from the ring into registers, reduced within the
+// CTA, and its gradient written from registers with 16-byte stores.
+constexpr int kRingThreads = 512;
+constexpr int kRingWarps = kRingThreads / 32;
+constexpr int kRingMaxDepth = 4;
+constexpr int64_t kRingSmemBudget = 220 * 1024;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeParams p, int depth) {
+  constexpr int EPV = 16 / sizeof(T);
+  extern __shared__ __align__(128) uint8_t ring_smem[];
+  __shared__ uint64_t full[kRingMaxDepth];
+  __shared__ float s_red[kRingWarps];
+  __shared__ int s_last, s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
+  const uint32_t buf_stride = (row_bytes + 127u) & ~127u;
+  const int64_t stride = gridDim.x;
+  const int64_t mine = p.N > blockIdx.x ? (p.N - 1 - blockIdx.x) / stride + 1 : 0;
+  const T* x = static_cast<const T*>(p.logits);
+  T* g = static_cast<T*>(p.grad);
+  const uint32_t ring_base = smem_addr(ring_smem);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < depth; ++i) mbar_init(smem_addr(&full[i]), 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&s_abort, p.status, 2000000000ull};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < depth && i < mine; ++i) {
+      const int64_t row = blockIdx.x + i * stride;
+      mbar_arrive_expect_tx(smem_addr(&full[i]), row_bytes);
+      bulk_load(ring_base + i * buf_stride, x + row * p.V, row_bytes, smem_addr(&full[i]));
+    }
+  }
+  grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
+  const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
+
+  for (int64_t j = 0; j < mine; ++j) {
+    const int b = static_cast<int>(j % depth);
+    const uint32_t parity = static_cast<uint32_t>((j / depth) & 1);
+    const int64_t row = blockIdx.x + j * stride;
+    const bool ok = mbar_wait(smem_addr(&full[b]), parity, ctl);
+    if (__syncthreads_or(!ok)) {
+      // gave up: let every bulk load still in flight land before leaving
+      if (threadIdx.x == 0) {
+        const int64_t issued = mine < j + depth ? mine : j + depth;
+        for (int64_t q = j; q < issued; ++q)
+          mbar_wait_drain(smem_addr(&full[q % depth]), static_cast<uint32_t>((q / depth) & 1), 2000000000ull);
+      }
+      __syncthreads();
+      break;
+    }
+    uint4 v[VPT];
+    const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * buf_stride);
+    const int nvec = static_cast<int>(row_bytes / 16);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int vi = i * kRingThreads + threadIdx.x;
+      if (vi < nvec) v[i] = sbuf[vi];
+    }
+    __syncthreads();  // buffer b has been copied out by every thread
+    if (threadIdx.x == 0 && j + depth < mine) {
+      const int64_t nrow = row + depth * stride;
+      mbar_arrive_expect_tx(smem_addr(&full[b]), row_bytes);
+      bulk_load(ring_base + b * buf_stride, x + nrow * p.V, row_bytes, smem_addr(&full[b]));
+    }
+    // row max
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) {
+        const T* e = reinterpret_cast<const T*>(&v[i]);
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) m = fmaxf(m, to_f<T>(e[k]));
+      }
+    }
+    m = warp_max(m);
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    m = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kRingWarps; ++w) m = fmaxf(m, s_red[w]);
+    // row sum of exp
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) {
+        const T* e = reinterpret_cast<const T*>(&v[i]);
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) s += __expf(to_f<T>(e[k]) - m);
+      }
+    }
+    s = warp_sum(s);
+    __syncthreads();  // everyone has read the maxima before the slots are reused
+    if (lane == 0) s_red[warp] = s;
+    __syncthreads();
+    s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRingWarps; ++w) s += s_red[w];
+    const float lse = m + logf(s);
+    const int64_t t = p.target[row];
+    const bool valid = t != p.ignore_index && t >= 0 && t < p.V;
+    float scale = 0.f;
+    if (valid) {
+      if (p.reduction == FLCE_REDUCTION_MEAN)
+        scale = p.grad_scale / static_cast<float>(nv);
+      else if (p.reduction == FLCE_REDUCTION_SUM)
+        scale = p.grad_scale;
+      else
+        scale = p.grad_scale * (p.grad_out != nullptr ? p.grad_out[row] : 1.f);
+    }
+    float zt = 0.f;
+    bool found = false;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int vi = i * kRingThreads + threadIdx.x;
+      if (vi < nvec) {
+        Packet<T, EPV>& pk = *reinterpret_cast<Packet<T, EPV>*>(&v[i]);
+        const int64_t e = static_cast<int64_t>(vi) * EPV;
+        if (g == nullptr) {
+          find_target<T, EPV>(pk, e, valid ? t : -1, zt, found);
+        } else {
+          grad_packet<T, EPV>(pk, e, t, valid, scale, lse, zt, found);
+          __stcs(reinterpret_cast<uint4*>(g + row * p.V + e), v[i]);
+        }
+      }
+    }
+    if (found) p.loss_rows[row] = lse - zt;
+    if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+  }
+
+  if (p.loss_out != nullptr) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned int ticket = atomicAdd(p.ticket, 1u);
+      s_last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      double acc = 0.0;
+      for (int64_t i = threadIdx.x; i < p.N; i += kRingThreads) acc += static_cast<double>(__ldcg(p.loss_rows + i));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      __shared__ double s_acc[kRingWarps];
+      if (lane == 0) s_acc[warp] = acc;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double total = 0.0;
+#pragma unroll
+        for (int w = 0; w < kRingWarps; ++w) total += s_acc[w];
+        if (p.reduction == FLCE_REDUCTION_MEAN) {
+          const int n_valid = *p.n_valid;
+          p.loss_out[0] = n_valid > 0 ? static_cast<float>(total / n_valid) : __int_as_float(0x7fc00000);
+        } else {
+          p.loss_out[0] = static_cast<float>(total);
+        }
+      }
+    }
+  }
+}
+
+template <typename T, int VPT>
+cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, bool pdl, cudaStream_t s) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(ce_rows_ring_kernel<T, VPT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kRingSmemBudget + 1024));
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kRingThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  CeParams pc = p;
+  return cudaLaunchKernelEx(&cfg, ce_rows_ring_kernel<T, VPT>, pc, depth);
 }
 
 template <typename T, int EPV>
@@ -277,10 +552,43 @@ int64_t ce_vector_elems(int dtype, bool vector_path) {
   return vector_path ? (dtype == FLCE_DTYPE_BF16 ? 8 : 4) : 1;
 }
 
+// Row-ring form when rows fit (see above); 0 when it does not apply.
+int ce_ring_depth(int64_t V, int dtype, bool vector_path) {
+  if (!vector_path) return 0;
+  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_BF16 ? 2 : 4);
+  const int64_t stride = (row_bytes + 127) / 128 * 128;
+  if (row_bytes > 72 * 1024) return 0;
+  int64_t depth = kRingSmemBudget / stride;
+  if (depth > kRingMaxDepth) depth = kRingMaxDepth;
+  return depth >= 2 ? static_cast<int>(depth) : 0;
+}
+
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool pdl, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
   prof_begin(s, FLCE_KERNEL_CE_ROWS);
   cudaError_t e;
+  const int depth = ce_ring_depth(p.V, dtype, vector_path);
+  if (depth > 0) {
+    const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_BF16 ? 2 : 4);
+    const int64_t vecs = row_bytes / 16;
+    const int vpt = static_cast<int>((vecs + kRingThreads - 1) / kRingThreads);
+    const size_t smem = static_cast<size_t>(depth) * ((row_bytes + 127) / 128 * 128);
+    int grid = device_sm_count();
+    if (grid > p.N) grid = static_cast<int>(p.N);
+    if (dtype == FLCE_DTYPE_BF16) {
+      e = vpt <= 1   ? launch_ring_t<uint16_t, 1>(p, depth, grid, smem, pdl, s)
+          : vpt <= 2 ? launch_ring_t<uint16_t, 2>(p, depth, grid, smem, pdl, s)
+          : vpt <= 4 ? launch_ring_t<uint16_t, 4>(p, depth, grid, smem, pdl, s)
+                     : launch_ring_t<uint16_t, 8>(p, depth, grid, smem, pdl, s);
+    } else {
+      e = vpt <= 1   ? launch_ring_t<float, 1>(p, depth, grid, smem, pdl, s)
+          : vpt <= 2 ? launch_ring_t<float, 2>(p, depth, grid, smem, pdl, s)
+          : vpt <= 4 ? launch_ring_t<float, 4>(p, depth, grid, smem, pdl, s)
+                     : launch_ring_t<float, 8>(p, depth, grid, smem, pdl, s);
+    }
+    prof_end(s);
+    return e;
+  }
   if (dtype == FLCE_DTYPE_BF16)
     e = vector_path ? launch_ce_t<uint16_t, 8>(p, pdl, s) : launch_ce_t<uint16_t, 1>(p, pdl, s);
   else

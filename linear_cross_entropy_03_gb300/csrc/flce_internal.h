@@ -96,25 +96,33 @@ struct CeParams {
   int* status;
   int cluster;              // CTAs per row
   int64_t seg_len;          // elements per CTA segment (multiple of the vector width)
+  float* loss_out;          // sum / mean: the last CTA writes the reduced loss here (null: no reduction)
+  unsigned int* ticket;     // zeroed counter used to find the last CTA
 };
 
 // Header at the start of every workspace.
 struct WorkspaceHeader {
   int status;
   int n_valid;
-  int pad[2];
+  int pad[2];               // [0]: count kernel block ticket, [1]: CE kernel block ticket
   double loss_sum;
   unsigned int tile_counters[];  // two per chunk
 };
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
+// zero_header: one block zeroes the header itself (status when it is the
+// header's own, counts, tickets and `num_counters` tile counters) before
+// counting, so no memset is needed; otherwise the caller zeroes the header.
+constexpr int64_t kCountSingleBlockMax = 65536;
 cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
-                                 WorkspaceHeader* hdr, int num_counters, int clear_status,
+                                 WorkspaceHeader* hdr, int num_counters, int zero_header,
                                  int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
                                  cudaStream_t s);
 cudaError_t launch_gemm(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,
                         const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,
+                         const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_row_finalize(const RowParams& p, cudaStream_t s);
 cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s);
 cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,

@@ -1,0 +1,467 @@
+// Tensor-core contractions of the fused linear cross entropy, CTA-pair form.
+//
+// Same three products as gemm_tc.cu (torchtune post "Peak Performance,
+// Minimized Memory ...", Figure 1 "Fused Linear Cross Entropy", steps 2 and
+// 4) on 256 x 256 tiles computed by a pair of CTAs on two SMs with
+// tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and 128 columns of
+// B in its own shared memory, the pair's tensor cores read both halves, and
+// each CTA's tensor memory receives its 128 rows of the accumulator.  Per SM
+// this halves the operand bytes that TMA writes into shared memory and the
+// MMA reads back out, which is what limits the one-CTA 128 x 256 form.
+//
+// Roles (same in both CTAs unless noted):
+//   warp 0    TMA producer for this CTA's halves; in the leader CTA (rank 0)
+//             also the tile scheduler, which writes every tile id into both
+//             CTAs' rings
+//   warp 1    TMEM allocation for the pair; in the leader, the MMA issuer
+//   warps 2-5 epilogue of this CTA's 128 accumulator rows
+// Operand bytes of both CTAs complete on the leader's stage barriers; the
+// leader's tcgen05.commit arrives on the matching barriers of both CTAs.
+#include <math.h>
+
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr int kHalf = 128;                       // rows of A / columns of B per CTA
+constexpr int kStages2 = 6;
+constexpr int kStage2Bytes = 2 * kHalf * kBK * 2;  // A half + B half: 32 KB
+constexpr int kGemm2SmemBytes = kStages2 * kStage2Bytes + 1024 + 1024;
+constexpr int kRingConsumers2 = 1 + kEpiWarps + 1 + kEpiWarps;  // leader MMA + epi, peer producer + epi
+
+struct Tile2 {
+  int kind;  // 0 forward, 1 grad_H, 2 grad_W
+  int m0, n0, kblocks;
+};
+
+// Pair tiles: 256 rows of M, 256 columns of N.
+__device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams& p) {
+  Tile2 ti;
+  if (mode == kModeForward) {
+    ti.kind = 0;
+    ti.m0 = (t % p.f_num_m) * 256;
+    ti.n0 = (t / p.f_num_m) * kBN;
+    ti.kblocks = p.f_kblocks;
+  } else if (t < p.h_tiles) {
+    ti.kind = 1;
+    ti.m0 = (t % p.h_num_m) * 256;
+    ti.n0 = (t / p.h_num_m) * kBN;
+    ti.kblocks = p.h_kblocks;
+  } else {
+    const int u = t - p.h_tiles;
+    ti.kind = 2;
+    ti.n0 = (u % p.w_num_n) * kBN;
+    ti.m0 = (u / p.w_num_n) * 256;
+    ti.kblocks = p.w_kblocks;
+  }
+  return ti;
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  const bool ok = mbar_wait_cluster(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias, int lim) {
+  if (lim >= 32) {
+    const uint4* b4 = reinterpret_cast<const uint4*>(bias);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4 u = __ldg(b4 + g);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * g + 2 * i] += bf16_lo(w[i]);
+        x[8 * g + 2 * i + 1] += bf16_hi(w[i]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < lim) x[j] += __uint_as_float(static_cast<uint32_t>(__ldg(bias + j)) << 16);
+  }
+}
+
+// Epilogue of one tile for this warp's 32 accumulator rows (`rl` = row
+// within the pair tile of this thread).
+__device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl) {
+  if (ti.kind == 0) {
+    const int r = ti.m0 + rl;
+    const bool row_ok = r < p.c_len;
+    const int ncols = min(kBN, p.V - ti.n0);
+    int t_rel = -1;
+    if (row_ok) {
+      const int64_t tg = p.target[p.row0 + r];
+      if (tg >= ti.n0 && tg < ti.n0 + ncols) t_rel = static_cast<int>(tg - ti.n0);
+    }
+    uint16_t* zrow = p.zbuf + static_cast<int64_t>(row_ok ? r : 0) * p.ldz + ti.n0;
+    float m_run = -INFINITY, s32 = 0.f, s16 = 0.f;
+    for (int c = 0; c < kBN; c += 32) {
+      if (c >= ncols) break;
+      uint32_t v[32];
+      tmem_load_32cols(tbase + c, v);
+      tmem_load_wait();
+      float x[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+      const int lim = ncols - c;
+      if (p.bias != nullptr) add_bias32(x, p.bias + ti.n0 + c, lim);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < lim) cmax = fmaxf(cmax, x[j]);
+      const float m_new = fmaxf(m_run, cmax);
+      const float corr = __expf(m_run - m_new);
+      s32 *= corr;
+      s16 *= corr;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (2 * i < lim) {
+          s32 += __expf(x[2 * i] - m_new);
+          s16 += __expf(bf16_lo(pk[i]) - m_new);
+        }
+        if (2 * i + 1 < lim) {
+          s32 += __expf(x[2 * i + 1] - m_new);
+          s16 += __expf(bf16_hi(pk[i]) - m_new);
+        }
+      }
+      m_run = m_new;
+      if (t_rel >= c && t_rel < c + 32) {
+        float zt = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == t_rel - c) zt = x[j];
+        p.tgt_logit[r] = zt;
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4)
+          if (8 * g4 < lim)
+            *reinterpret_cast<uint4*>(zrow + c + 8 * g4) =
+                make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
+      }
+    }
+    if (row_ok) p.partials[static_cast<int64_t>(r) * p.nvt + ti.n0 / kBN] = make_float4(m_run, s32, s16, 0.f);
+  } else if (ti.kind == 1) {
+    const int r = ti.m0 + rl;
+    const bool row_ok = r < p.c_len;
+    const int ncols = min(kBN, p.H - ti.n0);
+    uint16_t* out = p.grad_hidden + (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
+    for (int c = 0; c < kBN; c += 32) {
+      if (c >= ncols) break;
+      uint32_t v[32];
+      tmem_load_32cols(tbase + c, v);
+      tmem_load_wait();
+      if (row_ok) {
+        const int lim = ncols - c;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4)
+          if (8 * g4 < lim)
+            *reinterpret_cast<uint4*>(out + c + 8 * g4) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * g4 + 0]), __uint_as_float(v[8 * g4 + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * g4 + 2]), __uint_as_float(v[8 * g4 + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * g4 + 4]), __uint_as_float(v[8 * g4 + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * g4 + 6]), __uint_as_float(v[8 * g4 + 7])));
+      }
+    }
+  } else {
+    const int vrow = ti.m0 + rl;
+    const bool row_ok = vrow < p.V;
+    const int ncols = min(kBN, p.H - ti.n0);
+    float* out = p.grad_weight + static_cast<int64_t>(row_ok ? vrow : 0) * p.H + ti.n0;
+    for (int c = 0; c < kBN; c += 32) {
+      if (c >= ncols) break;
+      uint32_t v[32];
+      tmem_load_32cols(tbase + c, v);
+      tmem_load_wait();
+      if (row_ok) {
+        float4* o4 = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          if (c + 4 * g < ncols) {
+            float4 a = make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                   __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+            if (!p.gw_store) {
+              const float4 b = o4[g];
+              a.x += b.x;
+              a.y += b.y;
+              a.z += b.z;
+              a.w += b.w;
+            }
+            o4[g] = a;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+                 const __grid_constant__ CUtensorMap tm_z, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* bar_area = smem_raw + (base - raw) + kStages2 * kStage2Bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
+  uint64_t* empty = full + kStages2;
+  uint64_t* tfull = empty + kStages2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* ring_full = tempty + 2;
+  uint64_t* ring_empty = ring_full + kTileRing;
+  uint64_t* done = ring_empty + kTileRing;
+  int* ring = reinterpret_cast<int*>(done + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + kTileRing);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_addr(&tfull[a]), 1);
+      mbar_init(smem_addr(&tempty[a]), 2 * kEpiWarps);
+    }
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(smem_addr(&ring_full[i]), 1);
+      mbar_init(smem_addr(&ring_empty[i]), kRingConsumers2);
+    }
+    mbar_init(smem_addr(done), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_h);
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_z);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------ producer (+ scheduler in the leader)
+    if (lane == 0) {
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, rphase = 0;
+      uint64_t issued = 0;
+      bool ok = true;
+      while (ok) {
+        int t;
+        if (leader) {
+          if (!mbar_wait_cluster(smem_addr(&ring_empty[slot]), rphase ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          t = static_cast<int>(atomicAdd(p.tile_counter, 1u));
+          if (t >= p.num_tiles) t = -1;
+          ring[slot] = t;
+          st_shared_cluster_u32(map_to_cta(smem_addr(&ring[slot]), 1), static_cast<uint32_t>(t));
+          mbar_arrive(smem_addr(&ring_full[slot]));
+          mbar_arrive_cluster(map_to_cta(smem_addr(&ring_full[slot]), 1));
+        } else {
+          if (!mbar_wait_cluster(smem_addr(&ring_full[slot]), rphase, ctl)) {
+            ok = false;
+            break;
+          }
+          t = ring[slot];
+          mbar_arrive_cluster(map_to_cta(smem_addr(&ring_empty[slot]), 0));
+        }
+        if (++slot == kTileRing) {
+          slot = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        const Tile2 ti = decode_tile2(MODE, t, p);
+        const int mh = ti.m0 + kHalf * static_cast<int>(rank);  // this CTA's rows of A
+        const int nh = ti.n0 + kHalf * static_cast<int>(rank);  // this CTA's columns of B
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          if (!mbar_wait_cluster(smem_addr(&empty[stage]), phase ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * kStage2Bytes;
+          const uint32_t sb = sa + kHalf * kBK * 2;
+          const uint32_t fb = map_to_cta(smem_addr(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), 2 * kStage2Bytes);
+          const int k0 = kb * kBK;
+          if (ti.kind == 0) {
+            const int r = static_cast<int>(p.row0) + mh;
+            tma_load_2d_pair(sa, &tm_h, fb, k0, r);
+            tma_load_2d_pair(sa + kBoxBytes, &tm_h, fb, k0, r + 64);
+            tma_load_2d_pair(sb, &tm_w, fb, k0, nh);
+            tma_load_2d_pair(sb + kBoxBytes, &tm_w, fb, k0, nh + 64);
+          } else if (ti.kind == 1) {
+            tma_load_2d_pair(sa, &tm_z, fb, k0, mh);
+            tma_load_2d_pair(sa + kBoxBytes, &tm_z, fb, k0, mh + 64);
+            tma_load_2d_pair(sb, &tm_w, fb, nh, k0);
+            tma_load_2d_pair(sb + kBoxBytes, &tm_w, fb, nh + 64, k0);
+          } else {
+            tma_load_2d_pair(sa, &tm_z, fb, mh, k0);
+            tma_load_2d_pair(sa + kBoxBytes, &tm_z, fb, mh + 64, k0);
+            const int r = static_cast<int>(p.row0) + k0;
+            tma_load_2d_pair(sb, &tm_h, fb, nh, r);
+            tma_load_2d_pair(sb + kBoxBytes, &tm_h, fb, nh + 64, r);
+          }
+          ++issued;
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // Drain: copies still in flight must land before the pair exits.
+        for (int s = 0; s < kStages2; ++s) {
+          if (issued > static_cast<uint64_t>(s)) {
+            const uint64_t uses = (issued - 1 - s) / kStages2 + 1;
+            mbar_wait_cluster_drain(smem_addr(&full[s]), static_cast<uint32_t>((uses - 1) & 1u), p.timeout_ns);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      int stage = 0, slot = 0, acc = 0;
+      uint32_t phase = 0, rphase = 0, aphase = 0;
+      for (;;) {
+        if (!mbar_wait(smem_addr(&ring_full[slot]), rphase, ctl)) break;
+        const int t = ring[slot];
+        mbar_arrive(smem_addr(&ring_empty[slot]));
+        if (++slot == kTileRing) {
+          slot = 0;
+          rphase ^= 1u;
+        }
+        if (t < 0) break;
+        const Tile2 ti = decode_tile2(MODE, t, p);
+        if (!mbar_wait_cluster(smem_addr(&tempty[acc]), aphase ^ 1u, ctl)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        const uint32_t idesc = ti.kind == 0   ? instr_desc_bf16(256, kBN, 0, 0)
+                               : ti.kind == 1 ? instr_desc_bf16(256, kBN, 0, 1)
+                                              : instr_desc_bf16(256, kBN, 1, 1);
+        bool aborted = false;
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          if (!mbar_wait_cluster(smem_addr(&full[stage]), phase, ctl)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = base + stage * kStage2Bytes;
+          const uint32_t sb = sa + kHalf * kBK * 2;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = ti.kind == 2 ? smem_desc(sa + k * 2048, 8192, 1024)
+                                             : smem_desc(sa + k * 32, 16, 1024);
+            const uint64_t bd = ti.kind == 0 ? smem_desc(sb + k * 32, 16, 1024)
+                                             : smem_desc(sb + k * 2048, 8192, 1024);
+            mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit_pair(smem_addr(&empty[stage]), 0x3);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        mma_commit_pair(smem_addr(&tfull[acc]), 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+      // Every MMA must finish (it reads both CTAs' shared memory and writes
+      // both CTAs' tensor memory) before either CTA frees anything.
+      mma_commit_pair(smem_addr(done), 0x3);
+      mbar_wait_cluster_drain(smem_addr(done), 0, p.timeout_ns);
+    } else if (lane == 0) {
+      mbar_wait_cluster_drain(smem_addr(done), 0, p.timeout_ns + 1000000000ull);
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int q = warp & 3;
+    const uint32_t leader_tempty0 = map_to_cta(smem_addr(&tempty[0]), 0);
+    const uint32_t leader_tempty1 = map_to_cta(smem_addr(&tempty[1]), 0);
+    int slot = 0, acc = 0;
+    uint32_t rphase = 0, aphase = 0;
+    for (;;) {
+      if (!warp_wait_cluster(smem_addr(&ring_full[slot]), rphase, ctl)) break;
+      const int t = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_addr(&ring_empty[slot]), 0));
+      if (++slot == kTileRing) {
+        slot = 0;
+        rphase ^= 1u;
+      }
+      if (t < 0) break;
+      const Tile2 ti = decode_tile2(MODE, t, p);
+      if (!warp_wait_cluster(smem_addr(&tfull[acc]), aphase, ctl)) break;
+      tc_fence_after_sync();
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      epilogue_tile(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its pair may still touch its memory
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+int gemm2_max_smem_ok() {
+  static int configured[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (configured[dev]) return 1;
+  if (cudaFuncSetAttribute(gemm2_kernel<kModeForward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGemm2SmemBytes) != cudaSuccess)
+    return 0;
+  if (cudaFuncSetAttribute(gemm2_kernel<kModeBackward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGemm2SmemBytes) != cudaSuccess)
+    return 0;
+  configured[dev] = 1;
+  return 1;
+}
+
+// grid: number of CTAs, even (two per tile pair).
+cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_z,
+                         const GemmParams& p, int grid, cudaStream_t s) {
+  if (!gemm2_max_smem_ok()) return cudaErrorInvalidConfiguration;
+  prof_begin(s, mode == kModeForward ? FLCE_KERNEL_GEMM_FWD : FLCE_KERNEL_GEMM_BWD);
+  if (mode == kModeForward)
+    gemm2_kernel<kModeForward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
+  else
+    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(s);
+  return e;
+}
+
+}  // namespace flce

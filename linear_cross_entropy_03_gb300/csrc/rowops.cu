@@ -24,8 +24,18 @@ constexpr int kCountThreads = 1024;
 __global__ void __launch_bounds__(kCountThreads)
     count_targets_kernel(const int64_t* __restrict__ target, int64_t N, int64_t V, int64_t ignore_index,
                          WorkspaceHeader* hdr, int* status, int32_t* n_valid_out, float* zero_a,
-                         int64_t zero_a_n) {
+                         int64_t zero_a_n, int zero_header, int num_counters) {
   grid_dependents_launch();
+  if (zero_header) {  // single block: clear the header first
+    if (threadIdx.x == 0) {
+      if (status == &hdr->status) hdr->status = 0;
+      hdr->pad[0] = 0;
+      hdr->pad[1] = 0;
+      hdr->loss_sum = 0.0;
+    }
+    for (int i = threadIdx.x; i < num_counters; i += blockDim.x) hdr->tile_counters[i] = 0u;
+    __syncthreads();
+  }
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_a_n; i += stride)
     zero_a[i] = 0.f;
@@ -50,11 +60,17 @@ __global__ void __launch_bounds__(kCountThreads)
   if (threadIdx.x == 0) {
     int total = 0;
     for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += s_cnt[w];
-    atomicAdd(&hdr->n_valid, total);
-    __threadfence();
-    const unsigned int ticket = atomicAdd(reinterpret_cast<unsigned int*>(&hdr->pad[0]), 1u);
-    s_last = ticket == gridDim.x - 1;
+    if (zero_header) {
+      hdr->n_valid = total;
+      if (n_valid_out != nullptr) *n_valid_out = total;
+    } else {
+      atomicAdd(&hdr->n_valid, total);
+      __threadfence();
+      const unsigned int ticket = atomicAdd(reinterpret_cast<unsigned int*>(&hdr->pad[0]), 1u);
+      s_last = ticket == gridDim.x - 1;
+    }
   }
+  if (zero_header) return;
   __syncthreads();
   if (s_last && threadIdx.x == 0 && n_valid_out != nullptr) {
     __threadfence();
@@ -257,15 +273,16 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaS
 }  // namespace
 
 cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
-                                 WorkspaceHeader* hdr, int /*num_counters*/, int /*clear_status*/,
+                                 WorkspaceHeader* hdr, int num_counters, int zero_header,
                                  int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
                                  cudaStream_t s) {
   const int64_t work = N > zero_a_n ? N : zero_a_n;
   int blocks = static_cast<int>((work + kCountThreads * 4 - 1) / (kCountThreads * 4));
   blocks = blocks < 1 ? 1 : (blocks > sm_count() ? sm_count() : blocks);
+  if (zero_header) blocks = 1;
   prof_begin(s, FLCE_KERNEL_COUNT_TARGETS);
-  count_targets_kernel<<<blocks, kCountThreads, 0, s>>>(target, N, V, ignore_index, hdr, status,
-                                                       n_valid_out, zero_a, zero_a_n);
+  count_targets_kernel<<<blocks, kCountThreads, 0, s>>>(target, N, V, ignore_index, hdr, status, n_valid_out,
+                                                       zero_a, zero_a_n, zero_header, num_counters);
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;

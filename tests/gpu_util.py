@@ -27,7 +27,7 @@ def host(t) -> np.ndarray:
 
 def run_flce(inp, *, reduction="mean", chunk=0, use_bias=True, grad_scale=1.0, grad_out=None,
              accumulate=False, grad_weight_init=None, grad_bias_init=None, ignore_index=None,
-             grads=True):
+             grads=True, keep_f32=False):
     h = dev_bf16(inp.hidden)
     w = dev_bf16(inp.weight)
     b = dev_bf16(inp.bias) if (use_bias and inp.bias is not None) else None
@@ -41,8 +41,11 @@ def run_flce(inp, *, reduction="mean", chunk=0, use_bias=True, grad_scale=1.0, g
         grad_weight=grads, grad_weight_out=gw0, grad_bias_out=gb0 if b is not None else None,
         accumulate=accumulate, row_stats=True)
     torch.cuda.synchronize()
-    res = {k: (host(v) if isinstance(v, torch.Tensor) and k not in ("status", "n_valid", "workspace") else v)
+    conv = (lambda x: x.float().cpu().numpy()) if keep_f32 else host
+    res = {k: (conv(v) if isinstance(v, torch.Tensor) and k not in ("status", "n_valid", "workspace") else v)
            for k, v in out.items() if v is not None}
+    if keep_f32 and "loss" in res and np.ndim(res["loss"]) == 0:
+        res["loss"] = float(res["loss"])
     res["status"] = int(out["status"].item())
     res["n_valid"] = int(out["n_valid"].item())
     return res
