@@ -269,6 +269,12 @@ def e2e_steps(step, host, dev, steps, warmup, barrier):
     return t0.elapsed_time(t1), h2d, d2h
 
 
+def aggregate_tokens_per_s(ms_local, tokens_per_rank, world, all_reduce_max):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    ms = all_reduce_max(ms_local)
+    return tokens_per_rank * world / (ms / 1e3), ms
+
+
 # --------------------------------------------------------------------- oracle
 def oracle_sample(inp, rows: int):
     """The fp64 oracle on the first `rows` tokens of the workload; returns seconds."""
@@ -397,14 +403,15 @@ def main():
     flce.flce_profile_disable()
     status = int(step.status.item())
 
-    ms_step = ms_total / args.steps
-    t = torch.tensor([ms_step], device=device)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = float(t.item())
+    def all_reduce_max(x):
+        t = torch.tensor([x], device=device)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
     n, h, v = WORKLOAD["n"], WORKLOAD["h"], WORKLOAD["v"]
-    value = n * ws / (ms_step / 1e3)
+    value, ms_step = aggregate_tokens_per_s(ms_total / args.steps, n, ws, all_reduce_max)
 
     prof = kernel_profile(flce, records)
     total_k = sum(tk for _, tk in prof.values())

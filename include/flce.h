@@ -67,7 +67,7 @@ typedef enum {
   FLCE_REDUCTION_MEAN = 2  /* sum / number of valid rows (NaN if 0)   */
 } flce_reduction_t;
 
-typedef enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 } flce_dtype_t;
+typedef enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1, FLCE_DTYPE_FP16 = 2 } flce_dtype_t;
 
 typedef enum {
   FLCE_OK = 0,
@@ -159,7 +159,7 @@ size_t ce_workspace_size(int64_t N, int64_t V, int dtype, int reduction);
 /*
  * ce_fwd_bwd -- loss and grad_logits of cross_entropy(logits, target).
  *
- *  logits        [N, V] of `dtype` (FLCE_DTYPE_BF16 or FLCE_DTYPE_FP32).
+ *  logits        [N, V] of `dtype` (FLCE_DTYPE_BF16, FLCE_DTYPE_FP16 or FLCE_DTYPE_FP32).
  *  grad_logits   [N, V] of `dtype` output: scale_n * (softmax - onehot), 0 for
  *                ignored rows.  May equal `logits` (in place: the logits are
  *                consumed) or be a separate buffer (logits left unchanged),
@@ -177,6 +177,69 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
                          float grad_scale, const float* grad_out_none, float* loss,
                          void* workspace, size_t workspace_bytes, int32_t* status_dev,
                          flce_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Vocabulary-parallel building blocks
+ * ------------------------------------------------------------------------
+ * When the vocabulary is split across shards (tensor parallelism: the
+ * vocabulary-parallel cross entropy and the fused lm_head + vocabulary-
+ * parallel CE that never builds the [S, B, V/tp] logits -- "Native
+ * Liger-Kernel integration in Megatron-LM", PR table and Roadmap item 2;
+ * DeepSpeed PR #8540 "Changes"), shard s holds vocabulary ids
+ * [vocab_offset, vocab_offset + V_shard).  The cross entropy needs, per row,
+ * the log-sum-exp over the whole vocabulary and the target logit; the caller
+ * combines the shards' partials (for example with an all-reduce):
+ *     lse = M + log(sum_s exp(lse_s - M)),  M = max_s lse_s
+ *     z_t = sum_s zt_s              (zt_s is 0 unless shard s holds the target)
+ * and then lets every shard form its own gradients from the combined values
+ * and per-row scales row_scale[n] = d(reduced loss)/d(loss_n) (0 for ignored
+ * rows), which the caller also forms (it knows the global valid count, the
+ * reduction and the upstream gradient).  The loss is lse - z_t per row.
+ * Targets are global ids; ignore_index marks ignored rows.
+ */
+
+/* Bytes of workspace for flce_vp_forward / flce_vp_backward on a chunk of C rows. */
+size_t flce_vp_workspace_size(int64_t C, int64_t H, int64_t V_shard);
+
+/* FLCE on one vocabulary shard, forward part, for one chunk of C tokens:
+ * projects hidden [C, H] with weight_shard [V_shard, H] (+ bias_shard) into
+ * the workspace (bf16) and writes per row lse_shard (fp32 logits), lse16_shard
+ * (their bf16 roundings; combine it the same way for the gradient) and
+ * target_logit_shard.  The workspace must then be passed, unchanged, to
+ * flce_vp_backward for the same chunk.  Alignment and H as flce_fwd_bwd. */
+flce_status_t flce_vp_forward(const void* hidden, const void* weight_shard, const void* bias_shard,
+                              const int64_t* target, int64_t C, int64_t H, int64_t V_shard,
+                              int64_t vocab_offset, int64_t ignore_index, float* lse_shard,
+                              float* lse16_shard, float* target_logit_shard, void* workspace,
+                              size_t workspace_bytes, int32_t* status_dev, flce_stream_t stream);
+
+/* FLCE on one vocabulary shard, backward part: with lse16 [C] combined over
+ * all shards and row_scale [C], forms the shard's logits gradient in the
+ * workspace, then grad_hidden_partial (fp32 [C, H], overwritten; the caller
+ * sums it over shards), grad_weight_shard (fp32 [V_shard, H]) and
+ * grad_bias_shard (fp32 [V_shard]); accumulate = 1 adds to the latter two.
+ * Any of the three outputs may be NULL. */
+flce_status_t flce_vp_backward(const void* hidden, const void* weight_shard, const int64_t* target,
+                               int64_t C, int64_t H, int64_t V_shard, int64_t vocab_offset,
+                               int64_t ignore_index, const float* lse16, const float* row_scale,
+                               float* grad_hidden_partial, float* grad_weight_shard,
+                               float* grad_bias_shard, int accumulate, void* workspace,
+                               size_t workspace_bytes, int32_t* status_dev, flce_stream_t stream);
+
+/* Cross entropy on a vocabulary shard of materialised logits [N, V_shard]:
+ * per-row partials lse_shard and target_logit_shard.  No workspace. */
+flce_status_t ce_vp_partials(const void* logits, int dtype, const int64_t* target, int64_t N,
+                             int64_t V_shard, int64_t vocab_offset, int64_t ignore_index,
+                             float* lse_shard, float* target_logit_shard, int32_t* status_dev,
+                             flce_stream_t stream);
+
+/* ... and the shard's gradient from the combined lse [N] and row_scale [N]:
+ * grad = row_scale * (softmax - onehot), written to grad_logits (may equal
+ * logits).  No workspace. */
+flce_status_t ce_vp_backward(const void* logits, int dtype, void* grad_logits, const int64_t* target,
+                             int64_t N, int64_t V_shard, int64_t vocab_offset, int64_t ignore_index,
+                             const float* lse, const float* row_scale, int32_t* status_dev,
+                             flce_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Cross entropy on logits without any caller-provided scratch
@@ -217,8 +280,8 @@ flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void* grad_logit
  * ------------------------------------------------------------------------ */
 
 /* Tensor-core kernel form used by flce_fwd_bwd calls enqueued afterwards:
- * FLCE_GEMM_SINGLE_CTA (128 x 256 tiles, one CTA per tile) or
- * FLCE_GEMM_CTA_PAIR (256 x 256 tiles on a pair of SMs, tcgen05 cta_group::2).
+ * FLCE_GEMM_CTA_PAIR (the default: 256 x 256 tiles on a pair of SMs, tcgen05
+ * cta_group::2) or FLCE_GEMM_SINGLE_CTA (128 x 256 tiles, one CTA per tile).
  * 0 selects the default.  Returns the form now in effect. */
 #define FLCE_GEMM_SINGLE_CTA 1
 #define FLCE_GEMM_CTA_PAIR 2

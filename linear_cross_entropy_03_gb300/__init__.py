@@ -18,13 +18,14 @@ __all__ = [
     "REDUCTIONS", "DTYPES", "STATUS_BIT_TARGET_RANGE", "STATUS_BIT_TIMEOUT", "KERNEL_NAMES",
     "library_path", "lib", "flce_status_string", "flce_version", "flce_default_chunk",
     "flce_workspace_size", "flce_fwd_bwd", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
+    "flce_vp_workspace_size", "flce_vp_forward", "flce_vp_backward", "ce_vp_partials", "ce_vp_backward",
     "flce_set_gemm_variant", "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
     "flce_profile_enable", "flce_profile_disable", "flce_profile_read",
     "fused_linear_cross_entropy", "cross_entropy", "FlceError",
 ]
 
 REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
-DTYPES = {"bf16": 0, "fp32": 1}
+DTYPES = {"bf16": 0, "fp32": 1, "fp16": 2}
 STATUS_BIT_TARGET_RANGE = 0x1
 STATUS_BIT_TIMEOUT = 0x2
 KERNEL_NAMES = ("count_targets", "gemm_forward", "row_finalize", "grad_logits", "gemm_backward",
@@ -51,6 +52,13 @@ _SIGNATURES = {
     "ce_fwd_bwd_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                           ctypes.c_float, _P, _P, _P, _P]),
     "flce_set_gemm_variant": (ctypes.c_int, [ctypes.c_int]),
+    "flce_vp_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "flce_vp_forward": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ,
+                                       _P, _P]),
+    "flce_vp_backward": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P,
+                                        ctypes.c_int, _P, _SZ, _P, _P]),
+    "ce_vp_partials": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "ce_vp_backward": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P]),
     "flce_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "flce_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_uint64, _P]),
     "flce_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -164,6 +172,45 @@ def ce_fwd_bwd_noalloc(logits, dtype, grad_logits, target, N, V, ignore_index, r
         _ptr(loss), _ptr(status_dev), _stream(stream))
 
 
+def _dt(dtype) -> int:
+    return DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def flce_vp_workspace_size(C: int, H: int, V_shard: int) -> int:
+    return lib().flce_vp_workspace_size(C, H, V_shard)
+
+
+def flce_vp_forward(hidden, weight_shard, bias_shard, target, C, H, V_shard, vocab_offset, ignore_index,
+                    lse_shard, lse16_shard, target_logit_shard, workspace, workspace_bytes, status_dev,
+                    stream=None) -> int:
+    return lib().flce_vp_forward(
+        _ptr(hidden), _ptr(weight_shard), _ptr(bias_shard), _ptr(target), C, H, V_shard, vocab_offset,
+        ignore_index, _ptr(lse_shard), _ptr(lse16_shard), _ptr(target_logit_shard), _ptr(workspace),
+        int(workspace_bytes), _ptr(status_dev), _stream(stream))
+
+
+def flce_vp_backward(hidden, weight_shard, target, C, H, V_shard, vocab_offset, ignore_index, lse16,
+                     row_scale, grad_hidden_partial, grad_weight_shard, grad_bias_shard, accumulate, workspace,
+                     workspace_bytes, status_dev, stream=None) -> int:
+    return lib().flce_vp_backward(
+        _ptr(hidden), _ptr(weight_shard), _ptr(target), C, H, V_shard, vocab_offset, ignore_index,
+        _ptr(lse16), _ptr(row_scale), _ptr(grad_hidden_partial), _ptr(grad_weight_shard), _ptr(grad_bias_shard),
+        int(accumulate), _ptr(workspace), int(workspace_bytes), _ptr(status_dev), _stream(stream))
+
+
+def ce_vp_partials(logits, dtype, target, N, V_shard, vocab_offset, ignore_index, lse_shard,
+                   target_logit_shard, status_dev, stream=None) -> int:
+    return lib().ce_vp_partials(_ptr(logits), _dt(dtype), _ptr(target), N, V_shard, vocab_offset, ignore_index,
+                                _ptr(lse_shard), _ptr(target_logit_shard), _ptr(status_dev), _stream(stream))
+
+
+def ce_vp_backward(logits, dtype, grad_logits, target, N, V_shard, vocab_offset, ignore_index, lse, row_scale,
+                   status_dev, stream=None) -> int:
+    return lib().ce_vp_backward(_ptr(logits), _dt(dtype), _ptr(grad_logits), _ptr(target), N, V_shard,
+                                vocab_offset, ignore_index, _ptr(lse), _ptr(row_scale), _ptr(status_dev),
+                                _stream(stream))
+
+
 GEMM_SINGLE_CTA = 1
 GEMM_CTA_PAIR = 2
 
@@ -266,7 +313,7 @@ def cross_entropy(logits, target, *, ignore_index: int = -100, reduction="mean",
     """
     import torch
     n, v = logits.shape
-    dt = {torch.bfloat16: "bf16", torch.float32: "fp32"}.get(logits.dtype)
+    dt = {torch.bfloat16: "bf16", torch.float32: "fp32", torch.float16: "fp16"}.get(logits.dtype)
     if dt is None:
         raise FlceError(2, "cross_entropy")
     red = _red(reduction)

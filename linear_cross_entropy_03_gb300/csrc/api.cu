@@ -20,10 +20,14 @@ namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
 constexpr size_t kAlign = 256;
-constexpr int64_t kDefaultChunkBudget = int64_t(1) << 30;  // bytes of bf16 chunk logits
+// Default chunk: the largest multiple of 256 tokens whose bf16 logits fit in
+// 2 GiB (8192 tokens at V = 128256, 4096 at V = 256000).  Larger chunks halve
+// the fp32 grad_weight read-modify-write passes and give the long grad_H
+// products more tiles; the scratch stays bounded by the chunk.
+constexpr int64_t kDefaultChunkBudget = int64_t(2) << 30;
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
-std::atomic<int> g_gemm_variant{FLCE_GEMM_SINGLE_CTA};
+std::atomic<int> g_gemm_variant{FLCE_GEMM_CTA_PAIR};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -77,8 +81,8 @@ struct FlceLayout {
 
 int64_t default_chunk(int64_t N, int64_t V) {
   int64_t c = kDefaultChunkBudget / (V * 2);
-  c = c / 128 * 128;
-  if (c < 128) c = 128;
+  c = c / 256 * 256;
+  if (c < 256) c = 256;
   if (c > 16384) c = 16384;
   if (N > 0 && c > N) c = N;
   return c;
@@ -119,8 +123,8 @@ struct CeLayout {
 };
 
 bool ce_layout(int64_t N, int64_t V, int dtype, int reduction, CeLayout* L) {
-  if (N < 0 || V < 1 || (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32) || reduction < 0 ||
-      reduction > 2)
+  if (N < 0 || V < 1 || (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32 && dtype != FLCE_DTYPE_FP16) ||
+      reduction < 0 || reduction > 2)
     return false;
   L->header = 0;
   L->loss_rows = round_up(sizeof(WorkspaceHeader) + 16, kAlign);
@@ -327,13 +331,13 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
                          const float* grad_out_none, float* loss, void* workspace, size_t workspace_bytes,
                          int32_t* status_dev, flce_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32 && dtype != FLCE_DTYPE_FP16) return FLCE_ERR_UNSUPPORTED;
   CeLayout L;
   if (!ce_layout(N, V, dtype, reduction, &L)) return FLCE_ERR_INVALID_ARG;
   if (loss == nullptr || (N > 0 && (logits == nullptr || target == nullptr))) return FLCE_ERR_INVALID_ARG;
   if (grad_out_none != nullptr && reduction != FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARG;
   if (N >= (int64_t(1) << 31) / 8) return FLCE_ERR_UNSUPPORTED;
-  const size_t esz = dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  const size_t esz = dtype == FLCE_DTYPE_FP32 ? 4 : 2;
   if (!aligned(logits, esz) || !aligned(grad_logits, esz) || !aligned(target, 8) || !aligned(loss, 4))
     return FLCE_ERR_MISALIGNED;
   if (grad_logits != nullptr && grad_logits != logits) {
@@ -391,10 +395,221 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
 }
 
 int flce_set_gemm_variant(int variant) {
-  if (variant == 0) variant = FLCE_GEMM_SINGLE_CTA;
+  if (variant == 0) variant = FLCE_GEMM_CTA_PAIR;
   if (variant != FLCE_GEMM_SINGLE_CTA && variant != FLCE_GEMM_CTA_PAIR) return g_gemm_variant.load();
   g_gemm_variant.store(variant);
   return variant;
+}
+
+// ------------------------------------------------------------ vocabulary shards
+
+size_t flce_vp_workspace_size(int64_t C, int64_t H, int64_t V_shard) {
+  if (C < 1 || H < 8 || V_shard < 1 || C >= (int64_t(1) << 31) || V_shard >= (int64_t(1) << 31)) return 0;
+  FlceLayout L;
+  if (!flce_layout(C, H, V_shard, C, FLCE_REDUCTION_NONE, &L)) return 0;
+  return L.total;
+}
+
+flce_status_t flce_vp_forward(const void* hidden, const void* weight_shard, const void* bias_shard,
+                              const int64_t* target, int64_t C, int64_t H, int64_t V_shard, int64_t vocab_offset,
+                              int64_t ignore_index, float* lse_shard, float* lse16_shard,
+                              float* target_logit_shard, void* workspace, size_t workspace_bytes,
+                              int32_t* status_dev, flce_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (C < 1 || V_shard < 1 || H < 8 || vocab_offset < 0) return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  FlceLayout L;
+  if (!flce_layout(C, H, V_shard, C, FLCE_REDUCTION_NONE, &L)) return FLCE_ERR_INVALID_ARG;
+  if (hidden == nullptr || weight_shard == nullptr || target == nullptr || lse_shard == nullptr ||
+      lse16_shard == nullptr || target_logit_shard == nullptr)
+    return FLCE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(weight_shard, 16) || !aligned(bias_shard, 16) || !aligned(target, 8))
+    return FLCE_ERR_MISALIGNED;
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
+  int* status = status_dev != nullptr ? status_dev : &hdr->status;
+  FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WorkspaceHeader) + 4 * sizeof(unsigned int), stream));
+  CUtensorMap tm_h, tm_w, tm_z;
+  if (!make_map(&tm_h, hidden, H, C, H) || !make_map(&tm_w, weight_shard, H, V_shard, H) ||
+      !make_map(&tm_z, ws + L.zbuf, V_shard, C, L.vp))
+    return FLCE_ERR_CUDA;
+  const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
+  const int tile_m = pair ? 2 * kBM : kBM;
+  GemmParams g = {};
+  g.row0 = 0;
+  g.c_len = static_cast<int>(C);
+  g.H = static_cast<int>(H);
+  g.V = static_cast<int>(V_shard);
+  g.f_num_m = static_cast<int>(ceil_div(C, tile_m));
+  g.f_kblocks = static_cast<int>(ceil_div(H, kBK));
+  g.bias = static_cast<const uint16_t*>(bias_shard);
+  g.target = target;
+  g.v_offset = vocab_offset;
+  g.zbuf = reinterpret_cast<uint16_t*>(ws + L.zbuf);
+  g.ldz = L.vp;
+  g.partials = reinterpret_cast<float4*>(ws + L.partials);
+  g.nvt = static_cast<int>(L.nvt);
+  g.tgt_logit = reinterpret_cast<float*>(ws + L.tgt_logit);
+  g.status = status;
+  g.timeout_ns = g_timeout_ns.load();
+  g.num_tiles = static_cast<int>(g.f_num_m * L.nvt);
+  g.tile_counter = &hdr->tile_counters[0];
+  const int sms = device_sm_count();
+  if (pair)
+    FLCE_TRY_CUDA(launch_gemm2(kModeForward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
+  else
+    FLCE_TRY_CUDA(launch_gemm(kModeForward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+  RowParams r = {};
+  r.row0 = 0;
+  r.c_len = static_cast<int>(C);
+  r.N = C;
+  r.V = V_shard;
+  r.ignore_index = ignore_index;
+  r.target = target;
+  r.partials = g.partials;
+  r.nvt = g.nvt;
+  r.tgt_logit = g.tgt_logit;
+  r.v_offset = vocab_offset;
+  r.status = status;
+  FLCE_TRY_CUDA(launch_vp_finalize(r, lse_shard, lse16_shard, target_logit_shard, stream));
+  return FLCE_OK;
+}
+
+flce_status_t flce_vp_backward(const void* hidden, const void* weight_shard, const int64_t* target, int64_t C,
+                               int64_t H, int64_t V_shard, int64_t vocab_offset, int64_t ignore_index,
+                               const float* lse16, const float* row_scale, float* grad_hidden_partial,
+                               float* grad_weight_shard, float* grad_bias_shard, int accumulate, void* workspace,
+                               size_t workspace_bytes, int32_t* status_dev, flce_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (C < 1 || V_shard < 1 || H < 8 || vocab_offset < 0 || (accumulate != 0 && accumulate != 1))
+    return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  FlceLayout L;
+  if (!flce_layout(C, H, V_shard, C, FLCE_REDUCTION_NONE, &L)) return FLCE_ERR_INVALID_ARG;
+  if (hidden == nullptr || weight_shard == nullptr || target == nullptr || lse16 == nullptr || row_scale == nullptr)
+    return FLCE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(weight_shard, 16) || !aligned(target, 8) ||
+      !aligned(grad_hidden_partial, 16) || !aligned(grad_weight_shard, 16) || !aligned(grad_bias_shard, 4))
+    return FLCE_ERR_MISALIGNED;
+  if (workspace == nullptr || !aligned(workspace, kAlign) || workspace_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
+  int* status = status_dev != nullptr ? status_dev : &hdr->status;
+  FLCE_TRY_CUDA(cudaMemsetAsync(&hdr->tile_counters[1], 0, sizeof(unsigned int), stream));
+  if (grad_bias_shard != nullptr && !accumulate) FLCE_TRY_CUDA(launch_zero(grad_bias_shard, V_shard, stream));
+  RowParams r = {};
+  r.row0 = 0;
+  r.c_len = static_cast<int>(C);
+  r.N = C;
+  r.V = V_shard;
+  r.ignore_index = ignore_index;
+  r.target = target;
+  r.row_lse = const_cast<float*>(lse16);
+  r.row_scale = const_cast<float*>(row_scale);
+  r.row_tgt = nullptr;
+  r.v_offset = vocab_offset;
+  r.status = status;
+  r.zbuf = reinterpret_cast<uint16_t*>(ws + L.zbuf);
+  r.ldz = L.vp;
+  r.grad_bias = grad_bias_shard;
+  FLCE_TRY_CUDA(launch_grad_logits(r, stream));
+  if (grad_hidden_partial == nullptr && grad_weight_shard == nullptr) return FLCE_OK;
+  CUtensorMap tm_h, tm_w, tm_z;
+  if (!make_map(&tm_h, hidden, H, C, H) || !make_map(&tm_w, weight_shard, H, V_shard, H) ||
+      !make_map(&tm_z, ws + L.zbuf, V_shard, C, L.vp))
+    return FLCE_ERR_CUDA;
+  const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
+  const int tile_m = pair ? 2 * kBM : kBM;
+  GemmParams g = {};
+  g.row0 = 0;
+  g.c_len = static_cast<int>(C);
+  g.H = static_cast<int>(H);
+  g.V = static_cast<int>(V_shard);
+  g.target = target;
+  g.v_offset = vocab_offset;
+  g.zbuf = r.zbuf;
+  g.ldz = L.vp;
+  g.grad_hidden_f32 = grad_hidden_partial;
+  g.grad_weight = grad_weight_shard;
+  g.gw_store = accumulate ? 0 : 1;
+  g.status = status;
+  g.timeout_ns = g_timeout_ns.load();
+  g.h_num_m = static_cast<int>(ceil_div(C, tile_m));
+  g.h_kblocks = static_cast<int>(ceil_div(V_shard, kBK));
+  g.h_tiles = grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, kBN)) : 0;
+  g.w_num_n = static_cast<int>(ceil_div(H, kBN));
+  g.w_kblocks = static_cast<int>(ceil_div(C, kBK));
+  const int w_tiles = grad_weight_shard != nullptr ? static_cast<int>(ceil_div(V_shard, tile_m) * g.w_num_n) : 0;
+  g.num_tiles = g.h_tiles + w_tiles;
+  g.tile_counter = &hdr->tile_counters[1];
+  const int sms = device_sm_count();
+  if (pair)
+    FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
+  else
+    FLCE_TRY_CUDA(launch_gemm(kModeBackward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+  return FLCE_OK;
+}
+
+flce_status_t ce_vp_partials(const void* logits, int dtype, const int64_t* target, int64_t N, int64_t V_shard,
+                             int64_t vocab_offset, int64_t ignore_index, float* lse_shard, float* target_logit_shard,
+                             int32_t* status_dev, flce_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32 && dtype != FLCE_DTYPE_FP16) return FLCE_ERR_UNSUPPORTED;
+  if (N < 0 || V_shard < 1 || vocab_offset < 0) return FLCE_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 31) / 8) return FLCE_ERR_UNSUPPORTED;
+  if (N > 0 && (logits == nullptr || target == nullptr || lse_shard == nullptr || target_logit_shard == nullptr))
+    return FLCE_ERR_INVALID_ARG;
+  const size_t esz = dtype == FLCE_DTYPE_FP32 ? 4 : 2;
+  if (!aligned(logits, esz) || !aligned(target, 8) || !aligned(lse_shard, 4) || !aligned(target_logit_shard, 4))
+    return FLCE_ERR_MISALIGNED;
+  if (N == 0) return FLCE_OK;
+  const bool vec = (static_cast<size_t>(V_shard) * esz) % 16 == 0 && aligned(logits, 16);
+  const int64_t cap = ce_cta_capacity(dtype, vec);
+  const int64_t epv = ce_vector_elems(dtype, vec);
+  int64_t cl = ceil_div(V_shard, cap);
+  cl = cl > 8 ? 8 : (cl < 1 ? 1 : cl);
+  int64_t seg = ceil_div(ceil_div(V_shard, cl), epv) * epv;
+  cl = ceil_div(V_shard, seg);
+  CeParams p = {};
+  p.logits = logits;
+  p.grad = nullptr;
+  p.target = target;
+  p.N = N;
+  p.V = V_shard;
+  p.ignore_index = ignore_index;
+  p.reduction = FLCE_REDUCTION_SUM;  // no scale is formed in this mode
+  p.grad_scale = 1.f;
+  p.status = status_dev;
+  p.cluster = static_cast<int>(cl);
+  p.seg_len = seg;
+  p.lse_out = lse_shard;
+  p.zt_out = target_logit_shard;
+  p.v_offset = vocab_offset;
+  FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, false, stream));
+  return FLCE_OK;
+}
+
+flce_status_t ce_vp_backward(const void* logits, int dtype, void* grad_logits, const int64_t* target, int64_t N,
+                             int64_t V_shard, int64_t vocab_offset, int64_t ignore_index, const float* lse,
+                             const float* row_scale, int32_t* status_dev, flce_stream_t stream_) {
+  (void)status_dev;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32 && dtype != FLCE_DTYPE_FP16) return FLCE_ERR_UNSUPPORTED;
+  if (N < 0 || V_shard < 1 || vocab_offset < 0) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (logits == nullptr || grad_logits == nullptr || target == nullptr || lse == nullptr ||
+                row_scale == nullptr))
+    return FLCE_ERR_INVALID_ARG;
+  const size_t esz = dtype == FLCE_DTYPE_FP32 ? 4 : 2;
+  if (!aligned(logits, esz) || !aligned(grad_logits, esz) || !aligned(target, 8)) return FLCE_ERR_MISALIGNED;
+  if (grad_logits != logits) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(grad_logits);
+    const uintptr_t bytes = static_cast<uintptr_t>(N) * V_shard * esz;
+    if (a < b + bytes && b < a + bytes) return FLCE_ERR_INVALID_ARG;
+  }
+  FLCE_TRY_CUDA(launch_ce_vp_grad(logits, grad_logits, dtype, target, N, V_shard, vocab_offset, ignore_index, lse,
+                                  row_scale, stream));
+  return FLCE_OK;
 }
 
 void flce_set_wait_timeout_ns(uint64_t timeout_ns) {

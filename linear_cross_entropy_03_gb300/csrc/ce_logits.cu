@@ -17,6 +17,8 @@
 // order (deterministic) and writes the result.  Segments longer than the
 // register capacity fall back to a two-read streaming loop.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "ptx.cuh"
@@ -39,8 +41,13 @@ __device__ __forceinline__ float to_f<uint16_t>(uint16_t v) {
   return __uint_as_float(static_cast<uint32_t>(v) << 16);
 }
 
+template <>
+__device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+
 template <typename T>
 __device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
 template <>
 __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <>
@@ -222,8 +229,9 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
     lse = m_cta + logf(s);
   }
 
-  const int64_t t = p.target[row];
-  const bool valid = t != p.ignore_index && t >= 0 && t < p.V;
+  const int64_t tg = p.target[row];
+  const int64_t t = tg - p.v_offset;  // the target's column in these logits
+  const bool valid = tg != p.ignore_index && t >= 0 && t < p.V;
   grid_dependency_wait();  // n_valid (and the zeroed ticket) come from the preceding count kernel
   float scale = 0.f;
   if (valid) {
@@ -280,8 +288,16 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
       }
     }
   }
-  if (found) p.loss_rows[row] = lse - zt;
-  if (!valid && seg == 0 && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+  if (p.lse_out != nullptr) {  // partials of a vocabulary shard
+    if (found) p.zt_out[row] = zt;
+    if (seg == 0 && threadIdx.x == 0) {
+      p.lse_out[row] = lse;
+      if (!valid) p.zt_out[row] = 0.f;
+    }
+  } else {
+    if (found) p.loss_rows[row] = lse - zt;
+    if (!valid && seg == 0 && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+  }
 
   if (p.loss_out != nullptr) {
     // sum / mean: the last CTA to finish adds the row losses in a fixed order
@@ -319,12 +335,12 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
 
 // ---------------------------------------------------------------------------
 // Row-ring form, for rows that fit in shared memory (V * sizeof(T) <= 72 KB,
-// 16-byte aligned rows): one persistent 512-thread CTA per SM takes rows
+// 16-byte aligned rows): one persistent 1024-thread CTA per SM takes rows
 // blockIdx.x, blockIdx.x + gridDim.x, ...; one thread keeps `depth` whole-row
 // TMA bulk loads in flight in a shared-memory ring, so the SM streams without
 // pause.  Each row is copied from the ring into registers, reduced within the
 // CTA, and its gradient written from registers with 16-byte stores.
-constexpr int kRingThreads = 512;
+constexpr int kRingThreads = 1024;
 constexpr int kRingWarps = kRingThreads / 32;
 constexpr int kRingMaxDepth = 4;
 constexpr int64_t kRingSmemBudget = 220 * 1024;
@@ -335,12 +351,127 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// Packet helpers of the row-ring form: a 16-byte vector of 8 bf16 or 4 fp32.
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T>
+__device__ __forceinline__ float vec_max(const uint4& v);
+template <>
+__device__ __forceinline__ float vec_max<uint16_t>(const uint4& v) {
+  // the max of bf16 values is one of them: take it in packed bf16x2
+  __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
+                             *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.z),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+  a = __hmax2(a, b);
+  return fmaxf(__low2float(a), __high2float(a));
+}
+template <>
+__device__ __forceinline__ float vec_max<__half>(const uint4& v) {
+  __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y));
+  const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w));
+  a = __hmax2(a, b);
+  return fmaxf(__low2float(a), __high2float(a));
+}
+template <>
+__device__ __forceinline__ float vec_max<float>(const uint4& v) {
+  return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+
+// Replaces every element z by exp(z - m) (given mL = m * log2 e) and returns their sum.
+template <typename T>
+__device__ __forceinline__ float vec_exp_inplace(uint4& v, float mL);
+template <>
+__device__ __forceinline__ float vec_exp_inplace<uint16_t>(uint4& v, float mL) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float a = ex2_approx(fmaf(bf16_lo(w[q]), kLog2e, -mL));
+    const float b = ex2_approx(fmaf(bf16_hi(w[q]), kLog2e, -mL));
+    s0 += a;
+    s1 += b;
+    w[q] = pack_bf16x2(a, b);
+  }
+  return s0 + s1;
+}
+template <>
+__device__ __forceinline__ float vec_exp_inplace<__half>(uint4& v, float mL) {
+  __half2* w = reinterpret_cast<__half2*>(&v);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 z = __half22float2(w[q]);
+    const float a = ex2_approx(fmaf(z.x, kLog2e, -mL));
+    const float b = ex2_approx(fmaf(z.y, kLog2e, -mL));
+    s0 += a;
+    s1 += b;
+    w[q] = __floats2half2_rn(a, b);
+  }
+  return s0 + s1;
+}
+template <>
+__device__ __forceinline__ float vec_exp_inplace<float>(uint4& v, float mL) {
+  float* f = reinterpret_cast<float*>(&v);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; q += 2) {
+    f[q] = ex2_approx(fmaf(f[q], kLog2e, -mL));
+    f[q + 1] = ex2_approx(fmaf(f[q + 1], kLog2e, -mL));
+    s0 += f[q];
+    s1 += f[q + 1];
+  }
+  return s0 + s1;
+}
+
+template <typename T>
+__device__ __forceinline__ void vec_scale(uint4& v, float factor);
+template <>
+__device__ __forceinline__ void vec_scale<uint16_t>(uint4& v, float factor) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w[q] = pack_bf16x2(bf16_lo(w[q]) * factor, bf16_hi(w[q]) * factor);
+}
+template <>
+__device__ __forceinline__ void vec_scale<__half>(uint4& v, float factor) {
+  __half2* w = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 z = __half22float2(w[q]);
+    w[q] = __floats2half2_rn(z.x * factor, z.y * factor);
+  }
+}
+template <>
+__device__ __forceinline__ void vec_scale<float>(uint4& v, float factor) {
+  float* f = reinterpret_cast<float*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) f[q] *= factor;
+}
+
+template <typename T>
+__device__ __forceinline__ float vec_get(const uint4& v, int k) {
+  const T* e = reinterpret_cast<const T*>(&v);
+  float r = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16 / static_cast<int>(sizeof(T)); ++j)
+    if (j == k) r = to_f<T>(e[j]);
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ void vec_set(uint4& v, int k, float val) {
+  T* e = reinterpret_cast<T*>(&v);
+#pragma unroll
+  for (int j = 0; j < 16 / static_cast<int>(sizeof(T)); ++j)
+    if (j == k) e[j] = from_f<T>(val);
+}
+
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeParams p, int depth) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t ring_smem[];
   __shared__ uint64_t full[kRingMaxDepth];
-  __shared__ float s_red[kRingWarps];
+  __shared__ float2 s_part[2][kRingWarps];  // per warp (max, sum of exp(z - max)); double-buffered by row
   __shared__ int s_last, s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
@@ -350,6 +481,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   const T* x = static_cast<const T*>(p.logits);
   T* g = static_cast<T*>(p.grad);
   const uint32_t ring_base = smem_addr(ring_smem);
+  const int nvec = static_cast<int>(row_bytes / 16);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < depth; ++i) mbar_init(smem_addr(&full[i]), 1);
@@ -368,14 +500,59 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
   const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
 
+  // per-row scalars of this CTA's next row, loaded ahead of its data
+  int64_t t_next = mine > 0 ? p.target[blockIdx.x] : 0;
+  float go_next = (mine > 0 && p.grad_out != nullptr) ? p.grad_out[blockIdx.x] : 1.f;
   for (int64_t j = 0; j < mine; ++j) {
     const int b = static_cast<int>(j % depth);
     const uint32_t parity = static_cast<uint32_t>((j / depth) & 1);
     const int64_t row = blockIdx.x + j * stride;
+    const int64_t t = t_next;
+    const float go = go_next;
+    if (j + 1 < mine) {
+      t_next = p.target[row + stride];
+      if (p.grad_out != nullptr) go_next = p.grad_out[row + stride];
+    }
+    // on a timeout the row is computed from whatever is in the buffer and
+    // dropped at the row barrier below, which is also the abort vote
     const bool ok = mbar_wait(smem_addr(&full[b]), parity, ctl);
+    uint4 v[VPT];
+    const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * buf_stride);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int vi = i * kRingThreads + threadIdx.x;
+      if (vi < nvec) v[i] = sbuf[vi];
+    }
+    // where the target sits: its column here, and which thread / vector / lane holds it
+    const int64_t tcl = t - p.v_offset;
+    const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
+    const int tcol = valid ? static_cast<int>(tcl) : -1;
+    const int tvec = valid ? tcol / EPV : -1;
+    const bool own_t = valid && (tvec % kRingThreads) == static_cast<int>(threadIdx.x);
+    float zt = 0.f;
+    if (own_t) {
+      const int t_i = tvec / kRingThreads, t_k = tcol % EPV;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i == t_i) zt = vec_get<T>(v[i], t_k);
+    }
+    // warp max, then exp(z - warp max) in place and its warp sum
+    float mw = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) mw = fmaxf(mw, vec_max<T>(v[i]));
+    mw = warp_max(mw);
+    const float mL = mw * kLog2e;
+    float sw = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) sw += vec_exp_inplace<T>(v[i], mL);
+    sw = warp_sum(sw);
+    if (lane == 0) s_part[j & 1][warp] = make_float2(mw, sw);
+    // one barrier per row: it publishes the partials, frees ring buffer b and
+    // carries the abort vote
     if (__syncthreads_or(!ok)) {
-      // gave up: let every bulk load still in flight land before leaving
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == 0) {  // every bulk load still in flight must land before leaving
         const int64_t issued = mine < j + depth ? mine : j + depth;
         for (int64_t q = j; q < issued; ++q)
           mbar_wait_drain(smem_addr(&full[q % depth]), static_cast<uint32_t>((q / depth) & 1), 2000000000ull);
@@ -383,56 +560,29 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       __syncthreads();
       break;
     }
-    uint4 v[VPT];
-    const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * buf_stride);
-    const int nvec = static_cast<int>(row_bytes / 16);
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kRingThreads + threadIdx.x;
-      if (vi < nvec) v[i] = sbuf[vi];
-    }
-    __syncthreads();  // buffer b has been copied out by every thread
     if (threadIdx.x == 0 && j + depth < mine) {
       const int64_t nrow = row + depth * stride;
       mbar_arrive_expect_tx(smem_addr(&full[b]), row_bytes);
       bulk_load(ring_base + b * buf_stride, x + nrow * p.V, row_bytes, smem_addr(&full[b]));
     }
-    // row max
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) {
-        const T* e = reinterpret_cast<const T*>(&v[i]);
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) m = fmaxf(m, to_f<T>(e[k]));
+    // every warp combines the warps' partials itself
+    const float2 q = lane < kRingWarps ? s_part[j & 1][lane] : make_float2(-INFINITY, 0.f);
+    const float M = warp_max(q.x);
+    const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
+    const float lse = M + logf(S);
+
+    if (p.lse_out != nullptr) {  // partials of a vocabulary shard
+      if (own_t) p.zt_out[row] = zt;
+      if (threadIdx.x == 0) {
+        p.lse_out[row] = lse;
+        if (!valid) p.zt_out[row] = 0.f;
       }
+      continue;
     }
-    m = warp_max(m);
-    if (lane == 0) s_red[warp] = m;
-    __syncthreads();
-    m = s_red[0];
-#pragma unroll
-    for (int w = 1; w < kRingWarps; ++w) m = fmaxf(m, s_red[w]);
-    // row sum of exp
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) {
-        const T* e = reinterpret_cast<const T*>(&v[i]);
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) s += __expf(to_f<T>(e[k]) - m);
-      }
-    }
-    s = warp_sum(s);
-    __syncthreads();  // everyone has read the maxima before the slots are reused
-    if (lane == 0) s_red[warp] = s;
-    __syncthreads();
-    s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kRingWarps; ++w) s += s_red[w];
-    const float lse = m + logf(s);
-    const int64_t t = p.target[row];
-    const bool valid = t != p.ignore_index && t >= 0 && t < p.V;
+    if (own_t) p.loss_rows[row] = lse - zt;
+    if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+    if (g == nullptr) continue;
+
     float scale = 0.f;
     if (valid) {
       if (p.reduction == FLCE_REDUCTION_MEAN)
@@ -440,26 +590,29 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       else if (p.reduction == FLCE_REDUCTION_SUM)
         scale = p.grad_scale;
       else
-        scale = p.grad_scale * (p.grad_out != nullptr ? p.grad_out[row] : 1.f);
+        scale = p.grad_scale * go;
     }
-    float zt = 0.f;
-    bool found = false;
+    // softmax = exp(z - warp max) * exp(warp max - M) / S: one multiply per
+    // element; the target element is formed again in fp32 from its logit
+    const float factor = scale * ex2_approx((mw - M) * kLog2e) / S;
+    T* grow = g + row * p.V;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int vi = i * kRingThreads + threadIdx.x;
-      if (vi < nvec) {
-        Packet<T, EPV>& pk = *reinterpret_cast<Packet<T, EPV>*>(&v[i]);
-        const int64_t e = static_cast<int64_t>(vi) * EPV;
-        if (g == nullptr) {
-          find_target<T, EPV>(pk, e, valid ? t : -1, zt, found);
-        } else {
-          grad_packet<T, EPV>(pk, e, t, valid, scale, lse, zt, found);
-          __stcs(reinterpret_cast<uint4*>(g + row * p.V + e), v[i]);
-        }
-      }
+      if (vi < nvec) vec_scale<T>(v[i], factor);
     }
-    if (found) p.loss_rows[row] = lse - zt;
-    if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+    if (own_t) {
+      const int t_i = tvec / kRingThreads, t_k = tcol % EPV;
+      const float dt = scale * (__expf(zt - lse) - 1.f);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i == t_i) vec_set<T>(v[i], t_k, dt);
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int vi = i * kRingThreads + threadIdx.x;
+      if (vi < nvec) __stcs(reinterpret_cast<uint4*>(grow) + vi, v[i]);
+    }
   }
 
   if (p.loss_out != nullptr) {
@@ -544,18 +697,18 @@ cudaError_t launch_ce_t(const CeParams& p, bool pdl, cudaStream_t s) {
 
 // Elements per CTA held in registers (the segment length the host aims for).
 int64_t ce_cta_capacity(int dtype, bool vector_path) {
-  const int64_t epv = vector_path ? (dtype == FLCE_DTYPE_BF16 ? 8 : 4) : 1;
+  const int64_t epv = vector_path ? (dtype == FLCE_DTYPE_FP32 ? 4 : 8) : 1;
   return static_cast<int64_t>(kCeThreads) * kCeVecs * epv;
 }
 
 int64_t ce_vector_elems(int dtype, bool vector_path) {
-  return vector_path ? (dtype == FLCE_DTYPE_BF16 ? 8 : 4) : 1;
+  return vector_path ? (dtype == FLCE_DTYPE_FP32 ? 4 : 8) : 1;
 }
 
 // Row-ring form when rows fit (see above); 0 when it does not apply.
 int ce_ring_depth(int64_t V, int dtype, bool vector_path) {
   if (!vector_path) return 0;
-  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_BF16 ? 2 : 4);
+  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
   const int64_t stride = (row_bytes + 127) / 128 * 128;
   if (row_bytes > 72 * 1024) return 0;
   int64_t depth = kRingSmemBudget / stride;
@@ -569,7 +722,7 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
   cudaError_t e;
   const int depth = ce_ring_depth(p.V, dtype, vector_path);
   if (depth > 0) {
-    const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_BF16 ? 2 : 4);
+    const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
     const int64_t vecs = row_bytes / 16;
     const int vpt = static_cast<int>((vecs + kRingThreads - 1) / kRingThreads);
     const size_t smem = static_cast<size_t>(depth) * ((row_bytes + 127) / 128 * 128);
@@ -580,6 +733,11 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
           : vpt <= 2 ? launch_ring_t<uint16_t, 2>(p, depth, grid, smem, pdl, s)
           : vpt <= 4 ? launch_ring_t<uint16_t, 4>(p, depth, grid, smem, pdl, s)
                      : launch_ring_t<uint16_t, 8>(p, depth, grid, smem, pdl, s);
+    } else if (dtype == FLCE_DTYPE_FP16) {
+      e = vpt <= 1   ? launch_ring_t<__half, 1>(p, depth, grid, smem, pdl, s)
+          : vpt <= 2 ? launch_ring_t<__half, 2>(p, depth, grid, smem, pdl, s)
+          : vpt <= 4 ? launch_ring_t<__half, 4>(p, depth, grid, smem, pdl, s)
+                     : launch_ring_t<__half, 8>(p, depth, grid, smem, pdl, s);
     } else {
       e = vpt <= 1   ? launch_ring_t<float, 1>(p, depth, grid, smem, pdl, s)
           : vpt <= 2 ? launch_ring_t<float, 2>(p, depth, grid, smem, pdl, s)
@@ -591,6 +749,8 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
   }
   if (dtype == FLCE_DTYPE_BF16)
     e = vector_path ? launch_ce_t<uint16_t, 8>(p, pdl, s) : launch_ce_t<uint16_t, 1>(p, pdl, s);
+  else if (dtype == FLCE_DTYPE_FP16)
+    e = vector_path ? launch_ce_t<__half, 8>(p, pdl, s) : launch_ce_t<__half, 1>(p, pdl, s);
   else
     e = vector_path ? launch_ce_t<float, 4>(p, pdl, s) : launch_ce_t<float, 1>(p, pdl, s);
   prof_end(s);

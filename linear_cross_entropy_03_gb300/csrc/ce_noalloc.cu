@@ -60,12 +60,12 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
                                             const float* grad_out_none, float* loss,
                                             int32_t* status_dev, flce_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP32 && dtype != FLCE_DTYPE_FP16) return FLCE_ERR_UNSUPPORTED;
   if (N < 0 || V < 1 || reduction < 0 || reduction > 2) return FLCE_ERR_INVALID_ARG;
   if (N > FLCE_NOALLOC_MAX_ROWS) return FLCE_ERR_UNSUPPORTED;  // beyond the static scratch
   if (loss == nullptr || (N > 0 && (logits == nullptr || target == nullptr))) return FLCE_ERR_INVALID_ARG;
   if (grad_out_none != nullptr && reduction != FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARG;
-  const size_t esz = dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  const size_t esz = dtype == FLCE_DTYPE_FP32 ? 4 : 2;
   if (!aligned_to(logits, esz) || !aligned_to(grad_logits, esz) || !aligned_to(target, 8) ||
       !aligned_to(loss, 4))
     return FLCE_ERR_MISALIGNED;

@@ -41,6 +41,7 @@ struct GemmParams {
   // forward epilogue
   const uint16_t* bias;     // bf16 [V] or null
   const int64_t* target;    // [N]
+  int64_t v_offset;         // global id of this weight's first vocabulary row (0 unless sharded)
   uint16_t* zbuf;           // bf16 [c_len, ldz] chunk logits
   int64_t ldz;
   float4* partials;         // [c_len, nvt]: (max, sum exp(z - max), same over bf16(z), 0)
@@ -48,6 +49,7 @@ struct GemmParams {
   float* tgt_logit;         // [c_len]
   // backward epilogue
   uint16_t* grad_hidden;    // bf16 [N, H] or null
+  float* grad_hidden_f32;   // fp32 [N, H] instead of grad_hidden (a shard's partial), or null
   float* grad_weight;       // fp32 [V, H] or null
   int gw_store;             // 1: overwrite grad_weight tiles, 0: add to them
   // scheduling / failure
@@ -70,8 +72,9 @@ struct RowParams {
   const float* tgt_logit;
   const int* n_valid;
   float* row_lse;           // [c_len]: log-sum-exp of the bf16 logits (softmax of dZ)
-  float* row_scale;         // [c_len]
-  int* row_tgt;             // [c_len]: target or -1 when ignored
+  float* row_scale;         // [c_len]: 0 for ignored rows
+  int* row_tgt;             // [c_len]: target column or -1; null: derived from target - v_offset
+  int64_t v_offset;         // global id of the first vocabulary column (0 unless sharded)
   float* loss_rows;         // [N] (workspace, or the loss output for NONE)
   float* lse_out;           // [N] or null
   float* tl_out;            // [N] or null
@@ -98,6 +101,9 @@ struct CeParams {
   int64_t seg_len;          // elements per CTA segment (multiple of the vector width)
   float* loss_out;          // sum / mean: the last CTA writes the reduced loss here (null: no reduction)
   unsigned int* ticket;     // zeroed counter used to find the last CTA
+  float* lse_out;           // partials mode (vocabulary shard): per-row LSE here, no gradient
+  float* zt_out;            // partials mode: target logit if the target is in this shard, else 0
+  int64_t v_offset;         // global id of this shard's first column
 };
 
 // Header at the start of every workspace.
@@ -125,6 +131,11 @@ cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& t
                          const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_row_finalize(const RowParams& p, cudaStream_t s);
 cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s);
+cudaError_t launch_vp_finalize(const RowParams& p, float* lse_out, float* lse16_out, float* zt_out,
+                               cudaStream_t s);
+cudaError_t launch_ce_vp_grad(const void* logits, void* grad, int dtype, const int64_t* target, int64_t N,
+                              int64_t V, int64_t v_offset, int64_t ignore_index, const float* lse,
+                              const float* row_scale, cudaStream_t s);
 cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,
                                float* loss, cudaStream_t s, bool pdl);
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);

@@ -38,9 +38,15 @@ struct Tile {
 __device__ __forceinline__ Tile decode_tile(int mode, int t, const GemmParams& p) {
   Tile ti;
   if (mode == kModeForward) {
+    // row tiles in groups of 32 (4096 tokens), vocabulary tiles varying
+    // slowest within a group: the hidden rows in use stay resident in L2
     ti.kind = 0;
-    ti.m0 = (t % p.f_num_m) * kBM;
-    ti.n0 = (t / p.f_num_m) * kBN;
+    const int num_n = p.num_tiles / p.f_num_m;
+    const int per_group = 32 * num_n;
+    const int grp = t / per_group, r = t % per_group;
+    const int gm = min(32, p.f_num_m - grp * 32);
+    ti.m0 = (grp * 32 + r % gm) * kBM;
+    ti.n0 = (r / gm) * kBN;
     ti.kblocks = p.f_kblocks;
   } else if (t < p.h_tiles) {
     ti.kind = 1;
@@ -152,6 +158,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ producer / scheduler
     if (lane == 0) {
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_stream = l2_policy_evict_first();
       int stage = 0, slot = 0;
       uint32_t phase = 0, rphase = 0;
       uint64_t issued = 0;
@@ -183,10 +191,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int k0 = kb * kBK;
           if (ti.kind == 0) {
             const int r = static_cast<int>(p.row0) + ti.m0;
-            tma_load_2d(sa, &tm_h, fb, k0, r);
-            tma_load_2d(sa + kBoxBytes, &tm_h, fb, k0, r + 64);
+            tma_load_2d_hint(sa, &tm_h, fb, k0, r, pol_keep);
+            tma_load_2d_hint(sa + kBoxBytes, &tm_h, fb, k0, r + 64, pol_keep);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * kBoxBytes, &tm_w, fb, k0, ti.n0 + 64 * j);
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d_hint(sb + j * kBoxBytes, &tm_w, fb, k0, ti.n0 + 64 * j, pol_stream);
           } else if (ti.kind == 1) {
             tma_load_2d(sa, &tm_z, fb, k0, ti.m0);
             tma_load_2d(sa + kBoxBytes, &tm_z, fb, k0, ti.m0 + 64);
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int ncols = min(kBN, p.V - ti.n0);
         int t_rel = -1;
         if (row_ok) {
-          const int64_t tg = p.target[p.row0 + r];
+          const int64_t tg = p.target[p.row0 + r] - p.v_offset;
           if (tg >= ti.n0 && tg < ti.n0 + ncols) t_rel = static_cast<int>(tg - ti.n0);
         }
         uint16_t* zrow = p.zbuf + static_cast<int64_t>(row_ok ? r : 0) * p.ldz + ti.n0;
@@ -351,18 +360,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int g4 = 0; g4 < 4; ++g4)
               if (8 * g4 < lim)
-                *reinterpret_cast<uint4*>(zrow + c + 8 * g4) =
-                    make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
+                __stcs(reinterpret_cast<uint4*>(zrow + c + 8 * g4),
+                       make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]));
           }
         }
         if (row_ok)
           p.partials[static_cast<int64_t>(r) * p.nvt + ti.n0 / kBN] = make_float4(m_run, s32, s16, 0.f);
       } else if (ti.kind == 1) {
-        // grad_H rows of the chunk, bf16, written once
+        // grad_H rows of the chunk, written once: bf16, or fp32 for a shard's partial
         const int r = ti.m0 + rl;
         const bool row_ok = r < p.c_len;
         const int ncols = min(kBN, p.H - ti.n0);
-        uint16_t* out = p.grad_hidden + (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
+        const int64_t off = (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
         for (int c = 0; c < kBN; c += 32) {
           if (c >= ncols) break;
           uint32_t v[32];
@@ -371,7 +380,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float x[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
-          if (row_ok) store_bf16_32(out + c, x, ncols - c);
+          if (!row_ok) continue;
+          if (p.grad_hidden_f32 != nullptr) {
+            float4* o4 = reinterpret_cast<float4*>(p.grad_hidden_f32 + off + c);
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4)
+              if (c + 4 * g4 < ncols) o4[g4] = make_float4(x[4 * g4], x[4 * g4 + 1], x[4 * g4 + 2], x[4 * g4 + 3]);
+          } else {
+            store_bf16_32(p.grad_hidden + off + c, x, ncols - c);
+          }
         }
       } else {
         // grad_W rows (vocabulary ids), fp32, overwrite or add

@@ -29,6 +29,8 @@ constexpr int kStages2 = 6;
 constexpr int kStage2Bytes = 2 * kHalf * kBK * 2;  // A half + B half: 32 KB
 constexpr int kGemm2SmemBytes = kStages2 * kStage2Bytes + 1024 + 1024;
 constexpr int kRingConsumers2 = 1 + kEpiWarps + 1 + kEpiWarps;  // leader MMA + epi, peer producer + epi
+constexpr int kHGroup = 8;  // row tiles per group in the grad_H tile order
+constexpr int kFGroup = 16;  // row tiles per group in the forward tile order
 
 struct Tile2 {
   int kind;  // 0 forward, 1 grad_H, 2 grad_W
@@ -39,14 +41,26 @@ struct Tile2 {
 __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams& p) {
   Tile2 ti;
   if (mode == kModeForward) {
+    // row tiles in groups of kFGroup (4096 tokens), vocabulary tiles varying
+    // slowest within a group: the hidden rows in use stay resident in L2
     ti.kind = 0;
-    ti.m0 = (t % p.f_num_m) * 256;
-    ti.n0 = (t / p.f_num_m) * kBN;
+    const int num_n = p.num_tiles / p.f_num_m;
+    const int per_group = kFGroup * num_n;
+    const int grp = t / per_group, r = t % per_group;
+    const int gm = min(kFGroup, p.f_num_m - grp * kFGroup);
+    ti.m0 = (grp * kFGroup + r % gm) * 256;
+    ti.n0 = (r / gm) * kBN;
     ti.kblocks = p.f_kblocks;
   } else if (t < p.h_tiles) {
+    // grad_H tiles (K = V, long) in groups of kHGroup row tiles, columns
+    // varying within a group: the pairs running at once share fewer rows of
+    // dZ and columns of W, so fewer of them are re-read from DRAM
     ti.kind = 1;
-    ti.m0 = (t % p.h_num_m) * 256;
-    ti.n0 = (t / p.h_num_m) * kBN;
+    const int per_group = kHGroup * (p.h_tiles / p.h_num_m);
+    const int grp = t / per_group, r = t % per_group;
+    const int gm = min(kHGroup, p.h_num_m - grp * kHGroup);
+    ti.m0 = (grp * kHGroup + r % gm) * 256;
+    ti.n0 = (r / gm) * kBN;
     ti.kblocks = p.h_kblocks;
   } else {
     const int u = t - p.h_tiles;
@@ -92,7 +106,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
     const int ncols = min(kBN, p.V - ti.n0);
     int t_rel = -1;
     if (row_ok) {
-      const int64_t tg = p.target[p.row0 + r];
+      const int64_t tg = p.target[p.row0 + r] - p.v_offset;
       if (tg >= ti.n0 && tg < ti.n0 + ncols) t_rel = static_cast<int>(tg - ti.n0);
     }
     uint16_t* zrow = p.zbuf + static_cast<int64_t>(row_ok ? r : 0) * p.ldz + ti.n0;
@@ -141,8 +155,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4)
           if (8 * g4 < lim)
-            *reinterpret_cast<uint4*>(zrow + c + 8 * g4) =
-                make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
+            __stcs(reinterpret_cast<uint4*>(zrow + c + 8 * g4),
+                   make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]));
       }
     }
     if (row_ok) p.partials[static_cast<int64_t>(r) * p.nvt + ti.n0 / kBN] = make_float4(m_run, s32, s16, 0.f);
@@ -150,13 +164,21 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
     const int r = ti.m0 + rl;
     const bool row_ok = r < p.c_len;
     const int ncols = min(kBN, p.H - ti.n0);
-    uint16_t* out = p.grad_hidden + (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
+    const int64_t off = (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
+    uint16_t* out = p.grad_hidden + off;
     for (int c = 0; c < kBN; c += 32) {
       if (c >= ncols) break;
       uint32_t v[32];
       tmem_load_32cols(tbase + c, v);
       tmem_load_wait();
-      if (row_ok) {
+      if (row_ok && p.grad_hidden_f32 != nullptr) {  // fp32 partial of a vocabulary shard
+        float4* o4 = reinterpret_cast<float4*>(p.grad_hidden_f32 + off + c);
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4)
+          if (c + 4 * g4 < ncols)
+            o4[g4] = make_float4(__uint_as_float(v[4 * g4]), __uint_as_float(v[4 * g4 + 1]),
+                                 __uint_as_float(v[4 * g4 + 2]), __uint_as_float(v[4 * g4 + 3]));
+      } else if (row_ok) {
         const int lim = ncols - c;
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4)
@@ -257,6 +279,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ producer (+ scheduler in the leader)
     if (lane == 0) {
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_stream = l2_policy_evict_first();
       int stage = 0, slot = 0;
       uint32_t phase = 0, rphase = 0;
       uint64_t issued = 0;
@@ -301,11 +325,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), 2 * kStage2Bytes);
           const int k0 = kb * kBK;
           if (ti.kind == 0) {
+            // the chunk's hidden rows are re-read by every vocabulary tile; the
+            // weight is streamed once per chunk
             const int r = static_cast<int>(p.row0) + mh;
-            tma_load_2d_pair(sa, &tm_h, fb, k0, r);
-            tma_load_2d_pair(sa + kBoxBytes, &tm_h, fb, k0, r + 64);
-            tma_load_2d_pair(sb, &tm_w, fb, k0, nh);
-            tma_load_2d_pair(sb + kBoxBytes, &tm_w, fb, k0, nh + 64);
+            tma_load_2d_pair_hint(sa, &tm_h, fb, k0, r, pol_keep);
+            tma_load_2d_pair_hint(sa + kBoxBytes, &tm_h, fb, k0, r + 64, pol_keep);
+            tma_load_2d_pair_hint(sb, &tm_w, fb, k0, nh, pol_stream);
+            tma_load_2d_pair_hint(sb + kBoxBytes, &tm_w, fb, k0, nh + 64, pol_stream);
           } else if (ti.kind == 1) {
             tma_load_2d_pair(sa, &tm_z, fb, k0, mh);
             tma_load_2d_pair(sa + kBoxBytes, &tm_z, fb, k0, mh + 64);

@@ -12,6 +12,7 @@
 //                  Memory ...", Figure 1, step 3; liger-kernel README
 //                  "Kernels", CrossEntropy item).
 //  loss_reduce     sum (or mean) of the per-row losses in a fixed order.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "ptx.cuh"
@@ -143,7 +144,13 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
   if (threadIdx.x < rows) {
     s_lse[threadIdx.x] = p.row_lse[r0 + threadIdx.x];
     s_scale[threadIdx.x] = p.row_scale[r0 + threadIdx.x];
-    s_tgt[threadIdx.x] = p.row_tgt[r0 + threadIdx.x];
+    if (p.row_tgt != nullptr) {
+      s_tgt[threadIdx.x] = p.row_tgt[r0 + threadIdx.x];
+    } else {  // vocabulary shard: the target's column here, or -1 if another shard holds it
+      const int64_t tg = p.target[p.row0 + r0 + threadIdx.x];
+      const int64_t tl = tg - p.v_offset;
+      s_tgt[threadIdx.x] = (tg != p.ignore_index && tl >= 0 && tl < p.V) ? static_cast<int>(tl) : -1;
+    }
   }
   __syncthreads();
   const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kGlCols + threadIdx.x * 8;
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
     uint4 in[kGlUnroll];
 #pragma unroll
     for (int u = 0; u < kGlUnroll; ++u) {
-      if (rr + u < rows && s_tgt[rr + u] >= 0)
+      if (rr + u < rows && s_scale[rr + u] != 0.f)
         in[u] = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(rr + u) * p.ldz));
       else
         in[u] = make_uint4(0, 0, 0, 0);
@@ -167,8 +174,8 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
       const int r = rr + u;
       if (r >= rows) break;
       uint4* dst = reinterpret_cast<uint4*>(base + static_cast<int64_t>(r) * p.ldz);
-      const int t = s_tgt[r];
-      if (t < 0) {
+      const int t = s_tgt[r];  // -1: no target column in this block of the vocabulary
+      if (s_scale[r] == 0.f) {  // ignored row (or zero upstream gradient): exact zeros
         __stcs(dst, make_uint4(0, 0, 0, 0));
         continue;
       }
@@ -198,6 +205,71 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (j < nval) atomicAdd(p.grad_bias + v0 + j, cs[j]);
+  }
+}
+
+// Per-row partials of one vocabulary shard after its forward products:
+// LSE over the shard's fp32 logits, LSE over their bf16 roundings, and the
+// target logit when the target lies in the shard (else 0).
+__global__ void __launch_bounds__(32 * kFinalizeWarps)
+    vp_finalize_kernel(const RowParams p, float* lse_out, float* lse16_out, float* zt_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kFinalizeWarps + warp;
+  if (r >= p.c_len) return;
+  const float4* pr = p.partials + static_cast<int64_t>(r) * p.nvt;
+  float m = -INFINITY;
+  for (int i = lane; i < p.nvt; i += 32) m = fmaxf(m, pr[i].x);
+  m = warp_max(m);
+  float s32 = 0.f, s16 = 0.f;
+  for (int i = lane; i < p.nvt; i += 32) {
+    const float4 q = pr[i];
+    const float e = __expf(q.x - m);
+    s32 += q.y * e;
+    s16 += q.z * e;
+  }
+  s32 = warp_sum(s32);
+  s16 = warp_sum(s16);
+  if (lane == 0) {
+    const int64_t n = p.row0 + r;
+    const int64_t tg = p.target[n];
+    const int64_t tl = tg - p.v_offset;
+    const bool here = tg != p.ignore_index && tl >= 0 && tl < p.V;
+    lse_out[n] = m + logf(s32);
+    lse16_out[n] = m + logf(s16);
+    zt_out[n] = here ? p.tgt_logit[r] : 0.f;
+  }
+}
+
+// Gradient of the cross entropy on one vocabulary shard of materialised
+// logits, given the row LSE over the whole vocabulary and the row scale:
+// dZ = scale * (exp(z - lse) - [column == target]), written in place or to a
+// separate buffer; rows with scale 0 get exact zeros.
+__device__ __forceinline__ float load_as_f(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
+__device__ __forceinline__ float load_as_f(const __half* p) { return __half2float(*p); }
+__device__ __forceinline__ float load_as_f(const float* p) { return *p; }
+__device__ __forceinline__ void store_f(uint16_t* p, float v) { *p = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu); }
+__device__ __forceinline__ void store_f(__half* p, float v) { *p = __float2half_rn(v); }
+__device__ __forceinline__ void store_f(float* p, float v) { *p = v; }
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    ce_vp_grad_kernel(const T* __restrict__ logits, T* grad, const int64_t* __restrict__ target, int64_t N, int64_t V,
+                      int64_t v_offset, int64_t ignore_index, const float* __restrict__ lse,
+                      const float* __restrict__ row_scale) {
+  for (int64_t row = blockIdx.y; row < N; row += gridDim.y) {
+  const int64_t tg = target[row];
+  const int64_t tl = tg - v_offset;
+  const int64_t t = (tg != ignore_index && tl >= 0 && tl < V) ? tl : -1;
+  const float sc = row_scale[row];
+  const float l = lse[row];
+  const T* x = logits + row * V;
+  T* g = grad + row * V;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < V;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float z = load_as_f(x + v);
+    const float d = sc == 0.f ? 0.f : sc * (__expf(z - l) - (v == t ? 1.f : 0.f));
+    store_f(g + v, d);
+  }
   }
 }
 
@@ -307,6 +379,39 @@ cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s) {
   void* args[] = {&pc};
   const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(grad_logits_kernel), grid,
                                    dim3(kGlThreads), args, s, false);
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_vp_finalize(const RowParams& p, float* lse_out, float* lse16_out, float* zt_out,
+                               cudaStream_t s) {
+  const int blocks = (p.c_len + kFinalizeWarps - 1) / kFinalizeWarps;
+  prof_begin(s, FLCE_KERNEL_ROW_FINALIZE);
+  vp_finalize_kernel<<<blocks, 32 * kFinalizeWarps, 0, s>>>(p, lse_out, lse16_out, zt_out);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(s);
+  return e;
+}
+
+cudaError_t launch_ce_vp_grad(const void* logits, void* grad, int dtype, const int64_t* target, int64_t N,
+                              int64_t V, int64_t v_offset, int64_t ignore_index, const float* lse,
+                              const float* row_scale, cudaStream_t s) {
+  if (N <= 0) return cudaSuccess;
+  int64_t bx = (V + 255) / 256;
+  if (bx > 64) bx = 64;
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(N < 65535 ? N : 65535));
+  prof_begin(s, FLCE_KERNEL_CE_ROWS);
+  if (dtype == FLCE_DTYPE_BF16)
+    ce_vp_grad_kernel<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(logits),
+                                                      static_cast<uint16_t*>(grad), target, N, V, v_offset,
+                                                      ignore_index, lse, row_scale);
+  else if (dtype == FLCE_DTYPE_FP16)
+    ce_vp_grad_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(logits), static_cast<__half*>(grad),
+                                                    target, N, V, v_offset, ignore_index, lse, row_scale);
+  else
+    ce_vp_grad_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(logits), static_cast<float*>(grad),
+                                                   target, N, V, v_offset, ignore_index, lse, row_scale);
+  const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;
 }

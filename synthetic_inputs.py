@@ -248,11 +248,13 @@ def make_flce_inputs(n: int, h: int, v: int, seed: int, *, h_std: float = 1.0,
 
 def make_ce_logits(n: int, v: int, seed: int, *, std: float = 2.0, dtype: str = "bf16",
                    ignore_frac: float = 0.05, ignore_index: int = IGNORE_INDEX):
-    """Materialised logits [n, v] ~ N(0, std^2) (bf16 bits or float32) and targets."""
+    """Materialised logits [n, v] ~ N(0, std^2) (bf16 bits, float16 or float32) and targets."""
     if dtype == "bf16":
         logits = normal_bf16(seed, _S_LOGITS, (n, v), std)
     elif dtype == "fp32":
         logits = normal_f32(seed, _S_LOGITS, (n, v), std)
+    elif dtype == "fp16":
+        logits = normal_f32(seed, _S_LOGITS, (n, v), std).astype(np.float16)
     else:
         raise ValueError(dtype)
     t = uniform_targets(seed, _S_TARGET, n, v)

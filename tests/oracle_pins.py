@@ -238,7 +238,7 @@ def pin_ce_on_logits(O):
     assert np.all(np.asarray(r["loss"])[valid] == math.log(v))
     r = O.ce_reference(np.full((n, v), 0.8125), t, reduction="none")
     assert np.abs(np.asarray(r["loss"])[valid] - math.log(v)).max() <= 4e-16 * 4
-    for dtype in ("bf16", "fp32"):
+    for dtype in ("bf16", "fp16", "fp32"):
         logits, tt = si.make_ce_logits(n, v, 21, std=2.0, dtype=dtype, ignore_frac=0.15)
         z64 = si.bf16_to_float32(logits).astype(np.float64) if dtype == "bf16" else logits.astype(np.float64)
         for red in REDUCTIONS:

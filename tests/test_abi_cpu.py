@@ -102,6 +102,7 @@ def test_workspace_grows_with_chunk_not_n_times_v(lib):
     assert flce.flce_workspace_size(n, h, v, 2048, "none") < ws    # no per-row loss buffer
     assert flce.flce_workspace_size(-1, h, v, 0, "sum") == 0
     c = flce.flce_default_chunk(16384, 4096, 128256)
-    assert c % 128 == 0 and c * 128256 * 2 <= (1 << 30)
+    assert c == 8192 and c * 128256 * 2 <= (2 << 30)
+    assert flce.flce_default_chunk(32768, 4096, 256000) == 4096
     assert flce.flce_default_chunk(100, 64, 1000) == 100
     assert flce.ce_workspace_size(1024, 32768, "bf16", "mean") < 16 * 1024

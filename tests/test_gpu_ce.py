@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 def _logits_dev(logits, dtype):
     if dtype == "bf16":
         return dev_bf16(logits)
-    return torch.from_numpy(logits).cuda()
+    return torch.from_numpy(logits).cuda()  # float32 or float16
 
 
 def _run(logits, t, dtype, reduction, *, in_place=False, want_grad=True, grad_scale=1.0, grad_out=None):
@@ -35,7 +35,7 @@ def _run(logits, t, dtype, reduction, *, in_place=False, want_grad=True, grad_sc
     return loss, grad, int(out["status"].item())
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("reduction", ["none", "sum", "mean"])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_ce_config_1024x32768(dtype, reduction, in_place):
@@ -53,7 +53,7 @@ def test_ce_config_1024x32768(dtype, reduction, in_place):
         assert np.all(loss[~ref["valid"]] == 0.0)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("n,v", [(37, 1000), (64, 8192), (5, 8191), (9, 100003), (3, 1), (20, 70000),
                                  (16, 262144)])
 def test_ce_shapes(dtype, n, v):
@@ -67,7 +67,7 @@ def test_ce_shapes(dtype, n, v):
     assert np.all(grad[~ref["valid"]] == 0.0)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 def test_ce_loss_only(dtype):
     logits, t = si.make_ce_logits(200, 5000, 4, dtype=dtype)
     ref = O.ce_reference(logits, t, reduction="sum")
