@@ -45,6 +45,43 @@ WORKLOAD = dict(name="llama3_8b", n=16384, h=4096, v=128256, reduction="mean")
 CE_WORKLOAD = dict(n=1024, v=32768)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM traffic of the backward GEMM launch, from an ncu capture summarised in
+# profiles/; used only while the kernel's sources are the ones captured.
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "gemm_backward_traffic_llama3_8b.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "linear_cross_entropy_03_gb300", "csrc", f)
+                  for f in ("gemm_tc2.cu", "ptx.cuh", "flce_internal.h")]
+
+
+def kernel_source_hash():
+    """First 16 hex digits of the sha256 over the backward GEMM's source files."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(chunk):
+    """dram read + write bytes per backward launch from the committed summary,
+    or None when the summary is missing, was taken at another chunk, or the
+    kernel's sources have changed since."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, val = line[2:].split(":", 1)
+            fields[k.strip()] = val.strip().strip("`")
+    try:
+        if fields.get("kernel sources sha256/16") != kernel_source_hash() or int(fields["chunk"]) != chunk:
+            return None
+        return int(fields["dram bytes per launch (mean)"])
+    except (KeyError, ValueError):
+        return None
+
 
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -215,15 +252,20 @@ def kernel_profile(flce, records):
 
 def ce_bandwidth(step, iters=20):
     """ce_fwd_bwd alone, L2 flushed (256 MB write) before every call.  Returns the
-    median time of the whole call and of its ce_rows kernel (library events)."""
+    median time of the whole call and of its ce_rows kernel (library events).
+    A short device sleep after the flush keeps the GPU busy while the host
+    enqueues the call, so the call's time excludes the host's launch cost."""
     import torch
     flce = step.flce
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=step.ws.device)
+    sleep = getattr(torch.cuda, "_sleep", None)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times, kernel = [], []
     for i in range(iters + 3):
-        flush.fill_(i & 0xFF)
         flce.flce_profile_enable(16)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.fill_(i & 0xFF)
+        if sleep is not None:
+            sleep(200000)
         a.record()
         step.ce_call()
         b.record()
@@ -429,8 +471,9 @@ def main():
         avg_ms = tot_ms / launches
         achieved = gemm_flops(dom) / (avg_ms / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        traffic = measured_traffic(chunk) if dom == "gemm_backward" else None
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops_sustained",
                 "flops_per_launch": gemm_flops(dom), "avg_launch_ms": round(avg_ms, 4)}
     step_flops = 6.0 * n * h * v

@@ -338,8 +338,8 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
 // 16-byte aligned rows): one persistent 1024-thread CTA per SM takes rows
 // blockIdx.x, blockIdx.x + gridDim.x, ...; one thread keeps `depth` whole-row
 // TMA bulk loads in flight in a shared-memory ring, so the SM streams without
-// pause.  Each row is copied from the ring into registers, reduced within the
-// CTA, and its gradient written from registers with 16-byte stores.
+// pause.  Each row is copied from the ring into registers, reduced, and its
+// gradient written from the registers with 16-byte stores.
 constexpr int kRingThreads = 1024;
 constexpr int kRingWarps = kRingThreads / 32;
 constexpr int kRingMaxDepth = 4;
@@ -351,21 +351,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-// Packet helpers of the row-ring form: a 16-byte vector of 8 bf16 or 4 fp32.
+// Packet helpers of the row-ring form: a 16-byte vector of 8 bf16 / fp16 or 4 fp32.
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <typename T>
 __device__ __forceinline__ float vec_max(const uint4& v);
-template <>
-__device__ __forceinline__ float vec_max<uint16_t>(const uint4& v) {
-  // the max of bf16 values is one of them: take it in packed bf16x2
-  __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
-                             *reinterpret_cast<const __nv_bfloat162*>(&v.y));
-  const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.z),
-                                   *reinterpret_cast<const __nv_bfloat162*>(&v.w));
-  a = __hmax2(a, b);
-  return fmaxf(__low2float(a), __high2float(a));
-}
 template <>
 __device__ __forceinline__ float vec_max<__half>(const uint4& v) {
   __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y));
@@ -378,74 +368,116 @@ __device__ __forceinline__ float vec_max<float>(const uint4& v) {
   return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
 }
 
-// Replaces every element z by exp(z - m) (given mL = m * log2 e) and returns their sum.
+// Max over the vectors i of v with i * step < limit.
+template <typename T, int VPT>
+__device__ __forceinline__ float vec_max_all(const uint4 (&v)[VPT], int limit, int step) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i)
+    if (i * step < limit) m = fmaxf(m, vec_max<T>(v[i]));
+  return m;
+}
+// bf16: the max of bf16 values is one of them, so it is taken exactly in one
+// running packed bf16x2 maximum, converted once at the end.
+template <int VPT>
+__device__ __forceinline__ float vec_max_all_bf16(const uint4 (&v)[VPT], int limit, int step) {
+  __nv_bfloat162 m = __float2bfloat162_rn(-INFINITY);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    if (i * step < limit) {
+      const __nv_bfloat162* w = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+      m = __hmax2(m, __hmax2(__hmax2(w[0], w[1]), __hmax2(w[2], w[3])));
+    }
+  }
+  return fmaxf(__low2float(m), __high2float(m));
+}
+template <>
+__device__ __forceinline__ float vec_max_all<uint16_t, 2>(const uint4 (&v)[2], int limit, int step) {
+  return vec_max_all_bf16<2>(v, limit, step);
+}
+template <>
+__device__ __forceinline__ float vec_max_all<uint16_t, 4>(const uint4 (&v)[4], int limit, int step) {
+  return vec_max_all_bf16<4>(v, limit, step);
+}
+template <>
+__device__ __forceinline__ float vec_max_all<uint16_t, 8>(const uint4 (&v)[8], int limit, int step) {
+  return vec_max_all_bf16<8>(v, limit, step);
+}
+template <>
+__device__ __forceinline__ float vec_max_all<uint16_t, 10>(const uint4 (&v)[10], int limit, int step) {
+  return vec_max_all_bf16<10>(v, limit, step);
+}
+
+// Replaces every element z by exp(z - m) and adds the exponentials into the
+// two lanes of `acc`; nmL = -m * log2 e in both lanes.  Packed fp32x2
+// arithmetic: one FMA and one add per two elements.
 template <typename T>
-__device__ __forceinline__ float vec_exp_inplace(uint4& v, float mL);
+__device__ __forceinline__ void vec_exp_acc(uint4& v, float2 nmL, float2& acc);
 template <>
-__device__ __forceinline__ float vec_exp_inplace<uint16_t>(uint4& v, float mL) {
+__device__ __forceinline__ void vec_exp_acc<uint16_t>(uint4& v, float2 nmL, float2& acc) {
   uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-  float s0 = 0.f, s1 = 0.f;
+  const float2 l2e = make_float2(kLog2e, kLog2e);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float a = ex2_approx(fmaf(bf16_lo(w[q]), kLog2e, -mL));
-    const float b = ex2_approx(fmaf(bf16_hi(w[q]), kLog2e, -mL));
-    s0 += a;
-    s1 += b;
-    w[q] = pack_bf16x2(a, b);
+    const float2 a = __ffma2_rn(make_float2(bf16_lo(w[q]), bf16_hi(w[q])), l2e, nmL);
+    const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    acc = __fadd2_rn(acc, e);
+    w[q] = pack_bf16x2(e.x, e.y);
   }
-  return s0 + s1;
 }
 template <>
-__device__ __forceinline__ float vec_exp_inplace<__half>(uint4& v, float mL) {
+__device__ __forceinline__ void vec_exp_acc<__half>(uint4& v, float2 nmL, float2& acc) {
   __half2* w = reinterpret_cast<__half2*>(&v);
-  float s0 = 0.f, s1 = 0.f;
+  const float2 l2e = make_float2(kLog2e, kLog2e);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float2 z = __half22float2(w[q]);
-    const float a = ex2_approx(fmaf(z.x, kLog2e, -mL));
-    const float b = ex2_approx(fmaf(z.y, kLog2e, -mL));
-    s0 += a;
-    s1 += b;
-    w[q] = __floats2half2_rn(a, b);
+    const float2 a = __ffma2_rn(__half22float2(w[q]), l2e, nmL);
+    const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    acc = __fadd2_rn(acc, e);
+    w[q] = __floats2half2_rn(e.x, e.y);
   }
-  return s0 + s1;
 }
 template <>
-__device__ __forceinline__ float vec_exp_inplace<float>(uint4& v, float mL) {
-  float* f = reinterpret_cast<float*>(&v);
-  float s0 = 0.f, s1 = 0.f;
+__device__ __forceinline__ void vec_exp_acc<float>(uint4& v, float2 nmL, float2& acc) {
+  float2* f = reinterpret_cast<float2*>(&v);
+  const float2 l2e = make_float2(kLog2e, kLog2e);
 #pragma unroll
-  for (int q = 0; q < 4; q += 2) {
-    f[q] = ex2_approx(fmaf(f[q], kLog2e, -mL));
-    f[q + 1] = ex2_approx(fmaf(f[q + 1], kLog2e, -mL));
-    s0 += f[q];
-    s1 += f[q + 1];
+  for (int q = 0; q < 2; ++q) {
+    const float2 a = __ffma2_rn(f[q], l2e, nmL);
+    f[q] = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    acc = __fadd2_rn(acc, f[q]);
   }
-  return s0 + s1;
 }
 
 template <typename T>
 __device__ __forceinline__ void vec_scale(uint4& v, float factor);
+// bf16 data: exp(z - max) is held in bf16 and the gradient is one packed
+// multiply per two elements (the result is stored in bf16 anyway; the factor
+// and the product are each rounded once; bf16 has fp32's exponent range).
 template <>
 __device__ __forceinline__ void vec_scale<uint16_t>(uint4& v, float factor) {
-  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+  __nv_bfloat162* w = reinterpret_cast<__nv_bfloat162*>(&v);
+  const __nv_bfloat162 f = __float2bfloat162_rn(factor);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) w[q] = pack_bf16x2(bf16_lo(w[q]) * factor, bf16_hi(w[q]) * factor);
+  for (int q = 0; q < 4; ++q) w[q] = __hmul2(w[q], f);
 }
 template <>
 __device__ __forceinline__ void vec_scale<__half>(uint4& v, float factor) {
+  // fp16's range cannot hold small factors: multiply in fp32
   __half2* w = reinterpret_cast<__half2*>(&v);
+  const float2 f2 = make_float2(factor, factor);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float2 z = __half22float2(w[q]);
-    w[q] = __floats2half2_rn(z.x * factor, z.y * factor);
+    const float2 z = __fmul2_rn(__half22float2(w[q]), f2);
+    w[q] = __floats2half2_rn(z.x, z.y);
   }
 }
 template <>
 __device__ __forceinline__ void vec_scale<float>(uint4& v, float factor) {
-  float* f = reinterpret_cast<float*>(&v);
+  float2* f = reinterpret_cast<float2*>(&v);
+  const float2 f2 = make_float2(factor, factor);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) f[q] *= factor;
+  for (int q = 0; q < 2; ++q) f[q] = __fmul2_rn(f[q], f2);
 }
 
 template <typename T>
@@ -466,14 +498,39 @@ __device__ __forceinline__ void vec_set(uint4& v, int k, float val) {
     if (j == k) e[j] = from_f<T>(val);
 }
 
+// Barrier of one thread group (named barrier `id`, `count` threads) that also
+// returns whether any of its threads passed cond = true.
+__device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool cond) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(cond)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Two independent groups of kGroupThreads threads share the CTA's ring and
+// take alternate rows, each synchronising on its own named barrier, so one
+// group's reductions and stores overlap the other's waits.
+constexpr int kRingGroups = 2;
+constexpr int kGroupThreads = kRingThreads / kRingGroups;
+constexpr int kGroupWarps = kGroupThreads / 32;
+
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeParams p, int depth) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t ring_smem[];
   __shared__ uint64_t full[kRingMaxDepth];
-  __shared__ float2 s_part[2][kRingWarps];  // per warp (max, sum of exp(z - max)); double-buffered by row
+  __shared__ float2 s_part[kRingGroups][2][kGroupWarps];  // per warp (max, sum of exp(z - max))
   __shared__ int s_last, s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / kGroupWarps, gwarp = warp % kGroupWarps;
+  const int gtid = threadIdx.x % kGroupThreads;
+  const uint32_t bar_id = 1 + grp;
   const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
   const uint32_t buf_stride = (row_bytes + 127u) & ~127u;
   const int64_t stride = gridDim.x;
@@ -500,27 +557,28 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
   const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
 
-  // per-row scalars of this CTA's next row, loaded ahead of its data
-  int64_t t_next = mine > 0 ? p.target[blockIdx.x] : 0;
-  float go_next = (mine > 0 && p.grad_out != nullptr) ? p.grad_out[blockIdx.x] : 1.f;
-  for (int64_t j = 0; j < mine; ++j) {
+  // this group's rows: j = grp, grp + 2, ...; per-row scalars loaded one row ahead
+  int64_t t_next = grp < mine ? p.target[blockIdx.x + grp * stride] : 0;
+  float go_next = (grp < mine && p.grad_out != nullptr) ? p.grad_out[blockIdx.x + grp * stride] : 1.f;
+  int iter = 0;
+  for (int64_t j = grp; j < mine; j += kRingGroups, ++iter) {
     const int b = static_cast<int>(j % depth);
     const uint32_t parity = static_cast<uint32_t>((j / depth) & 1);
     const int64_t row = blockIdx.x + j * stride;
     const int64_t t = t_next;
     const float go = go_next;
-    if (j + 1 < mine) {
-      t_next = p.target[row + stride];
-      if (p.grad_out != nullptr) go_next = p.grad_out[row + stride];
+    if (j + kRingGroups < mine) {
+      t_next = p.target[row + kRingGroups * stride];
+      if (p.grad_out != nullptr) go_next = p.grad_out[row + kRingGroups * stride];
     }
     // on a timeout the row is computed from whatever is in the buffer and
-    // dropped at the row barrier below, which is also the abort vote
-    const bool ok = mbar_wait(smem_addr(&full[b]), parity, ctl);
+    // dropped at the group barrier below, which is also the abort vote
+    const bool ok = mbar_wait_sleep(smem_addr(&full[b]), parity, ctl);
     uint4 v[VPT];
     const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * buf_stride);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kRingThreads + threadIdx.x;
+      const int vi = i * kGroupThreads + gtid;
       if (vi < nvec) v[i] = sbuf[vi];
     }
     // where the target sits: its column here, and which thread / vector / lane holds it
@@ -528,59 +586,54 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
     const int tcol = valid ? static_cast<int>(tcl) : -1;
     const int tvec = valid ? tcol / EPV : -1;
-    const bool own_t = valid && (tvec % kRingThreads) == static_cast<int>(threadIdx.x);
+    const bool own_t = valid && (tvec % kGroupThreads) == gtid;
     float zt = 0.f;
     if (own_t) {
-      const int t_i = tvec / kRingThreads, t_k = tcol % EPV;
+      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
 #pragma unroll
       for (int i = 0; i < VPT; ++i)
         if (i == t_i) zt = vec_get<T>(v[i], t_k);
     }
     // warp max, then exp(z - warp max) in place and its warp sum
-    float mw = -INFINITY;
+    const float mw = warp_max(vec_max_all<T, VPT>(v, nvec - gtid, kGroupThreads));
+    const float2 nmL = make_float2(-mw * kLog2e, -mw * kLog2e);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
-      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) mw = fmaxf(mw, vec_max<T>(v[i]));
-    mw = warp_max(mw);
-    const float mL = mw * kLog2e;
-    float sw = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i)
-      if (i * kRingThreads + static_cast<int>(threadIdx.x) < nvec) sw += vec_exp_inplace<T>(v[i], mL);
-    sw = warp_sum(sw);
-    if (lane == 0) s_part[j & 1][warp] = make_float2(mw, sw);
-    // one barrier per row: it publishes the partials, frees ring buffer b and
-    // carries the abort vote
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0) {  // every bulk load still in flight must land before leaving
-        const int64_t issued = mine < j + depth ? mine : j + depth;
-        for (int64_t q = j; q < issued; ++q)
+      if (i * kGroupThreads + gtid < nvec) vec_exp_acc<T>(v[i], nmL, acc);
+    const float sw = warp_sum(acc.x + acc.y);
+    if (lane == 0) s_part[grp][iter & 1][gwarp] = make_float2(mw, sw);
+    // one group barrier per row: it publishes the partials, frees ring buffer
+    // b and carries the abort vote
+    if (group_sync_or(bar_id, kGroupThreads, !ok)) {
+      if (gtid == 0) {  // bulk loads still in flight must land before leaving
+        for (int64_t q = j; q < mine && q < j + depth; ++q)
           mbar_wait_drain(smem_addr(&full[q % depth]), static_cast<uint32_t>((q / depth) & 1), 2000000000ull);
       }
-      __syncthreads();
+      s_abort = 1;
       break;
     }
-    if (threadIdx.x == 0 && j + depth < mine) {
+    if (gtid == 0 && j + depth < mine) {
       const int64_t nrow = row + depth * stride;
       mbar_arrive_expect_tx(smem_addr(&full[b]), row_bytes);
       bulk_load(ring_base + b * buf_stride, x + nrow * p.V, row_bytes, smem_addr(&full[b]));
     }
-    // every warp combines the warps' partials itself
-    const float2 q = lane < kRingWarps ? s_part[j & 1][lane] : make_float2(-INFINITY, 0.f);
+    // every warp combines the group's warp partials itself
+    const float2 q = lane < kGroupWarps ? s_part[grp][iter & 1][lane] : make_float2(-INFINITY, 0.f);
     const float M = warp_max(q.x);
     const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
     const float lse = M + logf(S);
 
     if (p.lse_out != nullptr) {  // partials of a vocabulary shard
       if (own_t) p.zt_out[row] = zt;
-      if (threadIdx.x == 0) {
+      if (gtid == 0) {
         p.lse_out[row] = lse;
         if (!valid) p.zt_out[row] = 0.f;
       }
       continue;
     }
     if (own_t) p.loss_rows[row] = lse - zt;
-    if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+    if (!valid && gtid == 0) p.loss_rows[row] = 0.f;
     if (g == nullptr) continue;
 
     float scale = 0.f;
@@ -594,15 +647,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     }
     // softmax = exp(z - warp max) * exp(warp max - M) / S: one multiply per
     // element; the target element is formed again in fp32 from its logit
-    const float factor = scale * ex2_approx((mw - M) * kLog2e) / S;
+    const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
     T* grow = g + row * p.V;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kRingThreads + threadIdx.x;
+      const int vi = i * kGroupThreads + gtid;
       if (vi < nvec) vec_scale<T>(v[i], factor);
     }
     if (own_t) {
-      const int t_i = tvec / kRingThreads, t_k = tcol % EPV;
+      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
       const float dt = scale * (__expf(zt - lse) - 1.f);
 #pragma unroll
       for (int i = 0; i < VPT; ++i)
@@ -610,7 +663,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     }
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kRingThreads + threadIdx.x;
+      const int vi = i * kGroupThreads + gtid;
       if (vi < nvec) __stcs(reinterpret_cast<uint4*>(grow) + vi, v[i]);
     }
   }
@@ -724,25 +777,25 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
   if (depth > 0) {
     const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
     const int64_t vecs = row_bytes / 16;
-    const int vpt = static_cast<int>((vecs + kRingThreads - 1) / kRingThreads);
+    const int vpt = static_cast<int>((vecs + kGroupThreads - 1) / kGroupThreads);
     const size_t smem = static_cast<size_t>(depth) * ((row_bytes + 127) / 128 * 128);
     int grid = device_sm_count();
     if (grid > p.N) grid = static_cast<int>(p.N);
     if (dtype == FLCE_DTYPE_BF16) {
-      e = vpt <= 1   ? launch_ring_t<uint16_t, 1>(p, depth, grid, smem, pdl, s)
-          : vpt <= 2 ? launch_ring_t<uint16_t, 2>(p, depth, grid, smem, pdl, s)
+      e = vpt <= 2   ? launch_ring_t<uint16_t, 2>(p, depth, grid, smem, pdl, s)
           : vpt <= 4 ? launch_ring_t<uint16_t, 4>(p, depth, grid, smem, pdl, s)
-                     : launch_ring_t<uint16_t, 8>(p, depth, grid, smem, pdl, s);
+          : vpt <= 8 ? launch_ring_t<uint16_t, 8>(p, depth, grid, smem, pdl, s)
+                     : launch_ring_t<uint16_t, 10>(p, depth, grid, smem, pdl, s);
     } else if (dtype == FLCE_DTYPE_FP16) {
-      e = vpt <= 1   ? launch_ring_t<__half, 1>(p, depth, grid, smem, pdl, s)
-          : vpt <= 2 ? launch_ring_t<__half, 2>(p, depth, grid, smem, pdl, s)
+      e = vpt <= 2   ? launch_ring_t<__half, 2>(p, depth, grid, smem, pdl, s)
           : vpt <= 4 ? launch_ring_t<__half, 4>(p, depth, grid, smem, pdl, s)
-                     : launch_ring_t<__half, 8>(p, depth, grid, smem, pdl, s);
+          : vpt <= 8 ? launch_ring_t<__half, 8>(p, depth, grid, smem, pdl, s)
+                     : launch_ring_t<__half, 10>(p, depth, grid, smem, pdl, s);
     } else {
-      e = vpt <= 1   ? launch_ring_t<float, 1>(p, depth, grid, smem, pdl, s)
-          : vpt <= 2 ? launch_ring_t<float, 2>(p, depth, grid, smem, pdl, s)
+      e = vpt <= 2   ? launch_ring_t<float, 2>(p, depth, grid, smem, pdl, s)
           : vpt <= 4 ? launch_ring_t<float, 4>(p, depth, grid, smem, pdl, s)
-                     : launch_ring_t<float, 8>(p, depth, grid, smem, pdl, s);
+          : vpt <= 8 ? launch_ring_t<float, 8>(p, depth, grid, smem, pdl, s)
+                     : launch_ring_t<float, 10>(p, depth, grid, smem, pdl, s);
     }
     prof_end(s);
     return e;

@@ -83,6 +83,37 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is
+// incomplete, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for threads that have nothing else to do meanwhile: they sleep in
+// try_wait (up to 20 us per poll) rather than spin, leaving the issue slots
+// to other warps.  Same limits and abort protocol.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t polls = 1;; ++polls) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*ctl.abort_flag) return false;
+    if (global_timer_ns() - t0 > ctl.timeout_ns || polls > (1u << 30)) {
+      *ctl.abort_flag = 1;
+      if (ctl.status != nullptr) atomicOr(ctl.status, FLCE_STATUS_BIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Same limit but ignores the abort flag: used while draining after an abort.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
