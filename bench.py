@@ -251,29 +251,43 @@ def kernel_profile(flce, records):
 
 
 def ce_bandwidth(step, iters=20):
-    """ce_fwd_bwd alone, L2 flushed (256 MB write) before every call.  Returns the
-    median time of the whole call and of its ce_rows kernel (library events).
-    A short device sleep after the flush keeps the GPU busy while the host
-    enqueues the call, so the call's time excludes the host's launch cost."""
+    """ce_fwd_bwd alone, L2 emptied before every call: a 256 MB buffer is
+    written, then another 256 MB read, so the call finds none of its data in
+    L2 and no dirty lines of the flush to write back.  A short device sleep
+    keeps the GPU busy while the host enqueues the call, so the call's time
+    excludes the host's launch cost.  Returns the median time of the whole
+    call (library profiling off) and of its ce_rows kernel (library events,
+    a separate loop)."""
     import torch
     flce = step.flce
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=step.ws.device)
+    clean = torch.zeros(64 << 20, dtype=torch.float32, device=step.ws.device)
     sleep = getattr(torch.cuda, "_sleep", None)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    times, kernel = [], []
-    for i in range(iters + 3):
-        flce.flce_profile_enable(16)
+
+    def empty_l2(i):
         flush.fill_(i & 0xFF)
+        clean.sum()
         if sleep is not None:
             sleep(200000)
+
+    times, kernel = [], []
+    for i in range(iters + 3):
+        empty_l2(i)
         a.record()
         step.ce_call()
         b.record()
         torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    for i in range(iters + 3):
+        flce.flce_profile_enable(16)
+        empty_l2(i)
+        step.ce_call()
+        torch.cuda.synchronize()
         rec = flce.flce_profile_read(16)
         flce.flce_profile_disable()
         if i >= 3:
-            times.append(a.elapsed_time(b))
             kernel.append(sum(ms for name, ms in rec if name == "ce_rows"))
     cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
     alg_bytes = 2 * cn * cv * 2 + 12 * cn
@@ -480,7 +494,17 @@ def main():
     kernels = {k: {"launches": c, "ms_total": round(tk, 3), "share": round(tk / total_k, 4)}
                for k, (c, tk) in sorted(prof.items(), key=lambda x: -x[1][1])}
 
-    ce_ms, ce_kernel_ms, ce_bytes = ce_bandwidth(step) if not args.only_flce else (float("nan"), float("nan"), 0)
+    # the CE leg runs alone after a short idle, so that the clock cut the power
+    # cap imposed during the GEMM loop has lifted; its own clocks are recorded
+    ce_clocks = None
+    if args.only_flce:
+        ce_ms, ce_kernel_ms, ce_bytes = float("nan"), float("nan"), 0
+    else:
+        time.sleep(0.5)
+        sampler = ClockSampler(local)
+        sampler.start()
+        ce_ms, ce_kernel_ms, ce_bytes = ce_bandwidth(step, iters=100)
+        ce_clocks = sampler.stop()
     ce_gbs = ce_bytes / (ce_ms / 1e3) / 1e9
     ce_kernel_gbs = ce_bytes / (ce_kernel_ms / 1e3) / 1e9 if ce_kernel_ms > 0 else float("nan")
 
@@ -515,8 +539,8 @@ def main():
                              "kernel": "ce_rows", "kernel_ms": round(ce_kernel_ms, 4),
                              "kernel_gbs": round(ce_kernel_gbs, 1),
                              "kernel_frac": round(ce_kernel_gbs / peaks.get("hbm_gbs", 6800.0), 4),
-                             "l2": "flushed before every call", "scope": "gbs/frac: whole ce_fwd_bwd call "
-                             "(count + ce_rows kernels); kernel_*: ce_rows alone"},
+                             "l2": "emptied before every call (256 MB written, then 256 MB read)", "scope": "gbs/frac: whole ce_fwd_bwd call "
+                             "(count + ce_rows kernels); kernel_*: ce_rows alone", "clocks": ce_clocks},
             "scratch": {"workspace_bytes": step.ws_bytes, "full_logits_bytes": n * v * 2,
                         "chunk": chunk, "chunks": n_chunks},
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

@@ -480,6 +480,22 @@ __device__ __forceinline__ void vec_scale<float>(uint4& v, float factor) {
   for (int q = 0; q < 2; ++q) f[q] = __fmul2_rn(f[q], f2);
 }
 
+// A vector of -inf in the element type.
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_vec();
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<uint16_t>() {
+  return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+}
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<__half>() {
+  return make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);
+}
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<float>() {
+  return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+
 template <typename T>
 __device__ __forceinline__ float vec_get(const uint4& v, int k) {
   const T* e = reinterpret_cast<const T*>(&v);
@@ -525,61 +541,88 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t ring_smem[];
   __shared__ uint64_t full[kRingMaxDepth];
+  __shared__ int s_issued[kRingMaxDepth];  // loads issued into each buffer so far
   __shared__ float2 s_part[kRingGroups][2][kGroupWarps];  // per warp (max, sum of exp(z - max))
   __shared__ int s_last, s_abort;
+  __shared__ float s_gsum[kRingGroups], s_gcomp[kRingGroups];  // per group: compensated sum of its row losses
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / kGroupWarps, gwarp = warp % kGroupWarps;
   const int gtid = threadIdx.x % kGroupThreads;
   const uint32_t bar_id = 1 + grp;
   const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
   const uint32_t buf_stride = (row_bytes + 127u) & ~127u;
-  const int64_t stride = gridDim.x;
-  const int64_t mine = p.N > blockIdx.x ? (p.N - 1 - blockIdx.x) / stride + 1 : 0;
-  const T* x = static_cast<const T*>(p.logits);
-  T* g = static_cast<T*>(p.grad);
+  // row ids fit in 32 bits: the host accepts N < 2^28
+  const int stride = gridDim.x;
+  const int n_rows = static_cast<int>(p.N);
+  const int mine = n_rows > static_cast<int>(blockIdx.x) ? (n_rows - 1 - static_cast<int>(blockIdx.x)) / stride + 1 : 0;
   const uint32_t ring_base = smem_addr(ring_smem);
   const int nvec = static_cast<int>(row_bytes / 16);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < depth; ++i) mbar_init(smem_addr(&full[i]), 1);
+    for (int i = 0; i < depth; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      s_issued[i] = 0;
+    }
     s_abort = 0;
+    for (int q = 0; q < kRingGroups; ++q) s_gsum[q] = s_gcomp[q] = 0.f;
     fence_barrier_init();
   }
   __syncthreads();
   const WaitCtl ctl{&s_abort, p.status, 2000000000ull};
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < depth && i < mine; ++i) {
-      const int64_t row = blockIdx.x + i * stride;
-      mbar_arrive_expect_tx(smem_addr(&full[i]), row_bytes);
-      bulk_load(ring_base + i * buf_stride, x + row * p.V, row_bytes, smem_addr(&full[i]));
+  // the first row of each group is requested at once, the rest of the ring
+  // once group 0's first row has landed: the first rows of all SMs then
+  // share the DRAM bandwidth with fewer other requests and arrive sooner
+  const int first = depth < kRingGroups ? depth : kRingGroups;
+  // issues row `row` into buffer `bi`; the count is raised first, so a drain
+  // that sees it waits for this copy
+  auto issue = [&](int bi, int row) {
+    volatile int* cnt = s_issued;
+    cnt[bi] = cnt[bi] + 1;
+    mbar_arrive_expect_tx(smem_addr(&full[bi]), row_bytes);
+    bulk_load(ring_base + bi * buf_stride, static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.V, row_bytes,
+              smem_addr(&full[bi]));
+  };
+  // waits (bounded) for the latest copy issued into every buffer
+  auto drain = [&]() {
+    volatile int* cnt = s_issued;
+    for (int bi = 0; bi < depth; ++bi) {
+      const int c = cnt[bi];
+      if (c > 0) mbar_wait_drain(smem_addr(&full[bi]), static_cast<uint32_t>((c - 1) & 1), 2000000000ull);
     }
-  }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < first && i < mine; ++i) issue(i, blockIdx.x + i * stride);
+  const bool full_rows = nvec == VPT * kGroupThreads;  // no vector past the row's end
   grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
   const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
 
-  // this group's rows: j = grp, grp + 2, ...; per-row scalars loaded one row ahead
-  int64_t t_next = grp < mine ? p.target[blockIdx.x + grp * stride] : 0;
-  float go_next = (grp < mine && p.grad_out != nullptr) ? p.grad_out[blockIdx.x + grp * stride] : 1.f;
+  // this group's rows: j = grp, grp + 2, ...; a row's scalars are loaded
+  // before its data is waited for
   int iter = 0;
-  for (int64_t j = grp; j < mine; j += kRingGroups, ++iter) {
-    const int b = static_cast<int>(j % depth);
+  for (int j = grp; j < mine; j += kRingGroups, ++iter) {
+    const int b = j % depth;
     const uint32_t parity = static_cast<uint32_t>((j / depth) & 1);
-    const int64_t row = blockIdx.x + j * stride;
-    const int64_t t = t_next;
-    const float go = go_next;
-    if (j + kRingGroups < mine) {
-      t_next = p.target[row + kRingGroups * stride];
-      if (p.grad_out != nullptr) go_next = p.grad_out[row + kRingGroups * stride];
-    }
+    const int row = blockIdx.x + j * stride;
+    const int64_t t = __ldg(p.target + row);
+    const float go = p.grad_out != nullptr ? __ldg(p.grad_out + row) : 1.f;
     // on a timeout the row is computed from whatever is in the buffer and
     // dropped at the group barrier below, which is also the abort vote
     const bool ok = mbar_wait_sleep(smem_addr(&full[b]), parity, ctl);
+    if (j == 0 && gtid == 0)  // group 0's first row is here: request the rest of the ring
+      for (int i = first; i < depth && i < mine; ++i) issue(i, blockIdx.x + i * stride);
+    // vectors past the row's end hold -inf: they add nothing to the max or the
+    // sum and are not stored, so the row's work below needs no per-vector branch
     uint4 v[VPT];
     const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * buf_stride);
+    if (full_rows) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kGroupThreads + gtid;
-      if (vi < nvec) v[i] = sbuf[vi];
+      for (int i = 0; i < VPT; ++i) v[i] = sbuf[i * kGroupThreads + gtid];
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int vi = i * kGroupThreads + gtid;
+        v[i] = vi < nvec ? sbuf[vi] : neg_inf_vec<T>();
+      }
     }
     // where the target sits: its column here, and which thread / vector / lane holds it
     const int64_t tcl = t - p.v_offset;
@@ -595,29 +638,22 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
         if (i == t_i) zt = vec_get<T>(v[i], t_k);
     }
     // warp max, then exp(z - warp max) in place and its warp sum
-    const float mw = warp_max(vec_max_all<T, VPT>(v, nvec - gtid, kGroupThreads));
-    const float2 nmL = make_float2(-mw * kLog2e, -mw * kLog2e);
+    const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
+    const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;  // a warp past the row's end: all -inf, sum 0
+    const float2 nmL = make_float2(nm, nm);
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < VPT; ++i)
-      if (i * kGroupThreads + gtid < nvec) vec_exp_acc<T>(v[i], nmL, acc);
+    for (int i = 0; i < VPT; ++i) vec_exp_acc<T>(v[i], nmL, acc);
     const float sw = warp_sum(acc.x + acc.y);
     if (lane == 0) s_part[grp][iter & 1][gwarp] = make_float2(mw, sw);
     // one group barrier per row: it publishes the partials, frees ring buffer
     // b and carries the abort vote
     if (group_sync_or(bar_id, kGroupThreads, !ok)) {
-      if (gtid == 0) {  // bulk loads still in flight must land before leaving
-        for (int64_t q = j; q < mine && q < j + depth; ++q)
-          mbar_wait_drain(smem_addr(&full[q % depth]), static_cast<uint32_t>((q / depth) & 1), 2000000000ull);
-      }
       s_abort = 1;
+      if (gtid == 0) drain();  // bulk loads still in flight must land before leaving
       break;
     }
-    if (gtid == 0 && j + depth < mine) {
-      const int64_t nrow = row + depth * stride;
-      mbar_arrive_expect_tx(smem_addr(&full[b]), row_bytes);
-      bulk_load(ring_base + b * buf_stride, x + nrow * p.V, row_bytes, smem_addr(&full[b]));
-    }
+    if (gtid == 0 && j + depth < mine) issue(b, row + depth * stride);
     // every warp combines the group's warp partials itself
     const float2 q = lane < kGroupWarps ? s_part[grp][iter & 1][lane] : make_float2(-INFINITY, 0.f);
     const float M = warp_max(q.x);
@@ -632,9 +668,18 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       }
       continue;
     }
-    if (own_t) p.loss_rows[row] = lse - zt;
-    if (!valid && gtid == 0) p.loss_rows[row] = 0.f;
-    if (g == nullptr) continue;
+    if (p.loss_out != nullptr) {  // sum / mean: the group adds its rows' losses in row order
+      if (own_t) {               // (ordered across rows by the group barriers)
+        const float y = (lse - zt) - s_gcomp[grp];
+        const float t2 = s_gsum[grp] + y;
+        s_gcomp[grp] = (t2 - s_gsum[grp]) - y;
+        s_gsum[grp] = t2;
+      }
+    } else {
+      if (own_t) p.loss_rows[row] = lse - zt;
+      if (!valid && gtid == 0) p.loss_rows[row] = 0.f;
+    }
+    if (p.grad == nullptr) continue;
 
     float scale = 0.f;
     if (valid) {
@@ -648,12 +693,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     // softmax = exp(z - warp max) * exp(warp max - M) / S: one multiply per
     // element; the target element is formed again in fp32 from its logit
     const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
-    T* grow = g + row * p.V;
+    T* grow = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kGroupThreads + gtid;
-      if (vi < nvec) vec_scale<T>(v[i], factor);
-    }
+    for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
     if (own_t) {
       const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
       const float dt = scale * (__expf(zt - lse) - 1.f);
@@ -661,16 +703,28 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       for (int i = 0; i < VPT; ++i)
         if (i == t_i) vec_set<T>(v[i], t_k, dt);
     }
+    uint4* gvec = reinterpret_cast<uint4*>(grow) + gtid;
+    if (full_rows) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kGroupThreads + gtid;
-      if (vi < nvec) __stcs(reinterpret_cast<uint4*>(grow) + vi, v[i]);
+      for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i * kGroupThreads + gtid < nvec) __stcs(gvec + i * kGroupThreads, v[i]);
     }
   }
+  // the other group gave up: copies it would have consumed must land first
+  if (gtid == 0 && *static_cast<volatile int*>(&s_abort)) drain();
 
+  // sum / mean: each CTA leaves its partial in loss_rows[blockIdx.x] (the
+  // per-row losses are not needed); the last CTA adds the partials in a fixed
+  // tree order, so the result does not depend on which CTA finishes last
   if (p.loss_out != nullptr) {
     __syncthreads();
     if (threadIdx.x == 0) {
+      float part = 0.f;
+      for (int q = 0; q < kRingGroups; ++q) part += s_gsum[q] - s_gcomp[q];
+      p.loss_rows[blockIdx.x] = part;
       __threadfence();
       const unsigned int ticket = atomicAdd(p.ticket, 1u);
       s_last = ticket == gridDim.x - 1;
@@ -678,22 +732,24 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     __syncthreads();
     if (s_last) {
       __threadfence();
-      double acc = 0.0;
-      for (int64_t i = threadIdx.x; i < p.N; i += kRingThreads) acc += static_cast<double>(__ldcg(p.loss_rows + i));
+      float acc = 0.f;
+      for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kRingThreads) acc += __ldcg(p.loss_rows + i);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      __shared__ double s_acc[kRingWarps];
+      __shared__ float s_acc[kRingWarps];
       if (lane == 0) s_acc[warp] = acc;
       __syncthreads();
-      if (threadIdx.x == 0) {
-        double total = 0.0;
+      if (warp == 0) {
+        float total = s_acc[lane];
 #pragma unroll
-        for (int w = 0; w < kRingWarps; ++w) total += s_acc[w];
-        if (p.reduction == FLCE_REDUCTION_MEAN) {
-          const int n_valid = *p.n_valid;
-          p.loss_out[0] = n_valid > 0 ? static_cast<float>(total / n_valid) : __int_as_float(0x7fc00000);
-        } else {
-          p.loss_out[0] = static_cast<float>(total);
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        if (lane == 0) {
+          if (p.reduction == FLCE_REDUCTION_MEAN) {
+            const int n_valid = *p.n_valid;
+            p.loss_out[0] = n_valid > 0 ? total / static_cast<float>(n_valid) : __int_as_float(0x7fc00000);
+          } else {
+            p.loss_out[0] = total;
+          }
         }
       }
     }
