@@ -31,6 +31,10 @@ constexpr int kGemm2SmemBytes = kStages2 * kStage2Bytes + 1024 + 1024;
 constexpr int kRingConsumers2 = 1 + kEpiWarps + 1 + kEpiWarps;  // leader MMA + epi, peer producer + epi
 constexpr int kHGroup = 8;  // row tiles per group in the grad_H tile order
 constexpr int kFGroup = 16;  // row tiles per group in the forward tile order
+#ifndef FLCE_W_GROUP
+#define FLCE_W_GROUP 8
+#endif
+constexpr int kWGroup = FLCE_W_GROUP;  // hidden-column tiles per group in the grad_W tile order
 
 struct Tile2 {
   int kind;  // 0 forward, 1 grad_H, 2 grad_W
@@ -63,10 +67,16 @@ __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams&
     ti.n0 = (r / gm) * kBN;
     ti.kblocks = p.h_kblocks;
   } else {
+    // grad_W tiles in groups of kWGroup hidden-column tiles, vocabulary rows
+    // varying slowest within a group: the columns of H_c in use stay in L2
+    // while dZ streams through once per group
     const int u = t - p.h_tiles;
     ti.kind = 2;
-    ti.n0 = (u % p.w_num_n) * kBN;
-    ti.m0 = (u / p.w_num_n) * 256;
+    const int per_group = kWGroup * (p.num_tiles - p.h_tiles) / p.w_num_n;
+    const int grp = u / per_group, r = u % per_group;
+    const int gn = min(kWGroup, p.w_num_n - grp * kWGroup);
+    ti.n0 = (grp * kWGroup + r % gn) * kBN;
+    ti.m0 = (r / gn) * 256;
     ti.kblocks = p.w_kblocks;
   }
   return ti;
@@ -207,14 +217,14 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
           if (c + 4 * g < ncols) {
             float4 a = make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
                                    __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
-            if (!p.gw_store) {
-              const float4 b = o4[g];
+            if (!p.gw_store) {  // read-add-write, streamed past L2's resident data
+              const float4 b = __ldcs(o4 + g);
               a.x += b.x;
               a.y += b.y;
               a.z += b.z;
               a.w += b.w;
             }
-            o4[g] = a;
+            __stcs(o4 + g, a);
           }
         }
       }
@@ -338,11 +348,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tma_load_2d_pair(sb, &tm_w, fb, nh, k0);
             tma_load_2d_pair(sb + kBoxBytes, &tm_w, fb, nh + 64, k0);
           } else {
-            tma_load_2d_pair(sa, &tm_z, fb, mh, k0);
-            tma_load_2d_pair(sa + kBoxBytes, &tm_z, fb, mh + 64, k0);
+            // grad_W: every tile re-reads the chunk's hidden rows (kept in L2);
+            // each dZ column panel serves only the tiles of one vocabulary row
+            // running side by side (streamed)
+            tma_load_2d_pair_hint(sa, &tm_z, fb, mh, k0, pol_stream);
+            tma_load_2d_pair_hint(sa + kBoxBytes, &tm_z, fb, mh + 64, k0, pol_stream);
             const int r = static_cast<int>(p.row0) + k0;
-            tma_load_2d_pair(sb, &tm_h, fb, nh, r);
-            tma_load_2d_pair(sb + kBoxBytes, &tm_h, fb, nh + 64, r);
+            tma_load_2d_pair_hint(sb, &tm_h, fb, nh, r, pol_keep);
+            tma_load_2d_pair_hint(sb + kBoxBytes, &tm_h, fb, nh + 64, r, pol_keep);
           }
           ++issued;
           if (++stage == kStages2) {
