@@ -306,7 +306,7 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
 def cross_entropy(logits, target, *, ignore_index: int = -100, reduction="mean", grad_scale: float = 1.0,
                   grad_out=None, in_place: bool = False, want_grad: bool = True, grad_out_buffer=None,
                   workspace=None, status=None, stream=None) -> dict:
-    """Loss and grad_logits of cross_entropy(logits, target) on [N, V] bf16/fp32 logits.
+    """Loss and grad_logits of cross_entropy(logits, target) on [N, V] bf16/fp16/fp32 logits.
 
     ``in_place`` writes the gradient over ``logits``.  Returns a dict with
     ``loss``, ``grad_logits`` (or None) and ``status``.
