@@ -302,7 +302,8 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
 
     g.h_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.h_kblocks = static_cast<int>(ceil_div(V, kBK));
-    g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, kBN)) : 0;
+    // the pair form computes grad_H in 256 x 512 tiles, the one-CTA form in 128 x 256
+    g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, pair ? 2 * kBN : kBN)) : 0;
     g.w_num_n = static_cast<int>(ceil_div(H, kBN));
     g.w_kblocks = static_cast<int>(ceil_div(c_len, kBK));
     const int w_tiles = grad_weight != nullptr ? static_cast<int>(ceil_div(V, tile_m) * g.w_num_n) : 0;
@@ -537,7 +538,8 @@ flce_status_t flce_vp_backward(const void* hidden, const void* weight_shard, con
   g.timeout_ns = g_timeout_ns.load();
   g.h_num_m = static_cast<int>(ceil_div(C, tile_m));
   g.h_kblocks = static_cast<int>(ceil_div(V_shard, kBK));
-  g.h_tiles = grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, kBN)) : 0;
+  g.h_tiles =
+      grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, pair ? 2 * kBN : kBN)) : 0;
   g.w_num_n = static_cast<int>(ceil_div(H, kBN));
   g.w_kblocks = static_cast<int>(ceil_div(C, kBK));
   const int w_tiles = grad_weight_shard != nullptr ? static_cast<int>(ceil_div(V_shard, tile_m) * g.w_num_n) : 0;

@@ -25,9 +25,15 @@ namespace flce {
 namespace {
 
 constexpr int kHalf = 128;                       // rows of A / columns of B per CTA
-constexpr int kStages2 = 6;
-constexpr int kStage2Bytes = 2 * kHalf * kBK * 2;  // A half + B half: 32 KB
-constexpr int kGemm2SmemBytes = kStages2 * kStage2Bytes + 1024 + 1024;
+// Forward: 6 stages of 32 KB (A half + B half).  Backward: 4 stages of 48 KB,
+// room for the two B halves of a wide grad_H tile (below).
+constexpr int kWide = 2 * kBN;  // columns of a wide grad_H tile: 512
+template <int MODE>
+constexpr int stages2() { return MODE == kModeForward ? 6 : 4; }
+template <int MODE>
+constexpr int stage2_bytes() { return (MODE == kModeForward ? 2 : 3) * kHalf * kBK * 2; }
+template <int MODE>
+constexpr int gemm2_smem_bytes() { return stages2<MODE>() * stage2_bytes<MODE>() + 1024 + 1024; }
 constexpr int kRingConsumers2 = 1 + kEpiWarps + 1 + kEpiWarps;  // leader MMA + epi, peer producer + epi
 constexpr int kHGroup = 8;  // row tiles per group in the grad_H tile order
 constexpr int kFGroup = 16;  // row tiles per group in the forward tile order
@@ -64,7 +70,7 @@ __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams&
     const int grp = t / per_group, r = t % per_group;
     const int gm = min(kHGroup, p.h_num_m - grp * kHGroup);
     ti.m0 = (grp * kHGroup + r % gm) * 256;
-    ti.n0 = (r / gm) * kBN;
+    ti.n0 = (r / gm) * kWide;
     ti.kblocks = p.h_kblocks;
   } else {
     // grad_W tiles in groups of kWGroup hidden-column tiles, vocabulary rows
@@ -239,6 +245,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  constexpr int kStages2 = stages2<MODE>();
+  constexpr int kStage2Bytes = stage2_bytes<MODE>();
   uint8_t* bar_area = smem_raw + (base - raw) + kStages2 * kStage2Bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
   uint64_t* empty = full + kStages2;
@@ -332,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t sa = base + stage * kStage2Bytes;
           const uint32_t sb = sa + kHalf * kBK * 2;
           const uint32_t fb = map_to_cta(smem_addr(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), 2 * kStage2Bytes);
+          if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), ti.kind == 1 ? 6 * kBoxBytes * 2 : 4 * kBoxBytes * 2);
           const int k0 = kb * kBK;
           if (ti.kind == 0) {
             // the chunk's hidden rows are re-read by every vocabulary tile; the
@@ -343,10 +351,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tma_load_2d_pair_hint(sb, &tm_w, fb, k0, nh, pol_stream);
             tma_load_2d_pair_hint(sb + kBoxBytes, &tm_w, fb, k0, nh + 64, pol_stream);
           } else if (ti.kind == 1) {
+            // wide tile: this CTA's 128 columns of each 256-column half of B
             tma_load_2d_pair(sa, &tm_z, fb, k0, mh);
             tma_load_2d_pair(sa + kBoxBytes, &tm_z, fb, k0, mh + 64);
             tma_load_2d_pair(sb, &tm_w, fb, nh, k0);
             tma_load_2d_pair(sb + kBoxBytes, &tm_w, fb, nh + 64, k0);
+            tma_load_2d_pair(sb + 2 * kBoxBytes, &tm_w, fb, nh + kBN, k0);
+            tma_load_2d_pair(sb + 3 * kBoxBytes, &tm_w, fb, nh + kBN + 64, k0);
           } else {
             // grad_W: every tile re-reads the chunk's hidden rows (kept in L2);
             // each dZ column panel serves only the tiles of one vocabulary row
@@ -389,9 +400,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         }
         if (t < 0) break;
         const Tile2 ti = decode_tile2(MODE, t, p);
-        if (!mbar_wait_cluster(smem_addr(&tempty[acc]), aphase ^ 1u, ctl)) break;
+        // a wide grad_H tile takes both accumulator buffers (all 512 columns),
+        // one per 256-column half, in the order the epilogue frees them
+        const int nbuf = ti.kind == 1 ? 2 : 1;
+        int bufs[2] = {0, 0};
+        bool got = true;
+        for (int q = 0; q < nbuf; ++q) {
+          if (!mbar_wait_cluster(smem_addr(&tempty[acc]), aphase ^ 1u, ctl)) {
+            got = false;
+            break;
+          }
+          bufs[q] = acc;
+          if (++acc == 2) {
+            acc = 0;
+            aphase ^= 1u;
+          }
+        }
+        if (!got) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(bufs[0] * kBN);
+        const uint32_t d_tmem1 = tmem_base + static_cast<uint32_t>(bufs[1] * kBN);
         const uint32_t idesc = ti.kind == 0   ? instr_desc_bf16(256, kBN, 0, 0)
                                : ti.kind == 1 ? instr_desc_bf16(256, kBN, 0, 1)
                                               : instr_desc_bf16(256, kBN, 1, 1);
@@ -411,6 +439,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const uint64_t bd = ti.kind == 0 ? smem_desc(sb + k * 32, 16, 1024)
                                              : smem_desc(sb + k * 2048, 8192, 1024);
             mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if (ti.kind == 1)  // second half of a wide tile: same A, the next two B boxes
+              mma_bf16_pair(d_tmem1, ad, smem_desc(sb + 2 * kBoxBytes + k * 2048, 8192, 1024), idesc,
+                            (kb | k) != 0 ? 1u : 0u);
           }
           mma_commit_pair(smem_addr(&empty[stage]), 0x3);
           if (++stage == kStages2) {
@@ -419,11 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (aborted) break;
-        mma_commit_pair(smem_addr(&tfull[acc]), 0x3);
-        if (++acc == 2) {
-          acc = 0;
-          aphase ^= 1u;
-        }
+        for (int q = 0; q < nbuf; ++q) mma_commit_pair(smem_addr(&tfull[bufs[q]]), 0x3);
       }
       // Every MMA must finish (it reads both CTAs' shared memory and writes
       // both CTAs' tensor memory) before either CTA frees anything.
@@ -449,19 +476,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         rphase ^= 1u;
       }
       if (t < 0) break;
-      const Tile2 ti = decode_tile2(MODE, t, p);
-      if (!warp_wait_cluster(smem_addr(&tfull[acc]), aphase, ctl)) break;
-      tc_fence_after_sync();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      epilogue_tile(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);
-      if (++acc == 2) {
-        acc = 0;
-        aphase ^= 1u;
+      Tile2 ti = decode_tile2(MODE, t, p);
+      // a wide grad_H tile arrives as two 256-column halves, one per buffer
+      const int nbuf = ti.kind == 1 ? 2 : 1;
+      bool ok = true;
+      for (int half = 0; half < nbuf; ++half) {
+        if (!warp_wait_cluster(smem_addr(&tfull[acc]), aphase, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t tbase =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+        epilogue_tile(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+        ti.n0 += kBN;
       }
+      if (!ok) break;
     }
   }
 
@@ -480,10 +517,10 @@ int gemm2_max_smem_ok() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (configured[dev]) return 1;
   if (cudaFuncSetAttribute(gemm2_kernel<kModeForward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGemm2SmemBytes) != cudaSuccess)
+                           gemm2_smem_bytes<kModeForward>()) != cudaSuccess)
     return 0;
   if (cudaFuncSetAttribute(gemm2_kernel<kModeBackward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGemm2SmemBytes) != cudaSuccess)
+                           gemm2_smem_bytes<kModeBackward>()) != cudaSuccess)
     return 0;
   configured[dev] = 1;
   return 1;
@@ -495,9 +532,9 @@ cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& t
   if (!gemm2_max_smem_ok()) return cudaErrorInvalidConfiguration;
   prof_begin(s, mode == kModeForward ? FLCE_KERNEL_GEMM_FWD : FLCE_KERNEL_GEMM_BWD);
   if (mode == kModeForward)
-    gemm2_kernel<kModeForward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
+    gemm2_kernel<kModeForward><<<grid, kGemmThreads, gemm2_smem_bytes<kModeForward>(), s>>>(tm_h, tm_w, tm_z, p);
   else
-    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
+    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, gemm2_smem_bytes<kModeBackward>(), s>>>(tm_h, tm_w, tm_z, p);
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;
