@@ -25,15 +25,17 @@ namespace flce {
 namespace {
 
 constexpr int kHalf = 128;                       // rows of A / columns of B per CTA
-// Forward: 6 stages of 32 KB (A half + B half).  Backward: 4 stages of 48 KB,
-// room for the two B halves of a wide grad_H tile (below).
+// The operand ring (192 KB) holds 6 stages of 32 KB (A half + B half), or,
+// while wide grad_H tiles run, 4 stages of 48 KB (A half + two B halves).
+// Producer and MMA issuer switch layouts at the same tile; the producer first
+// waits until the MMAs have released every stage.
 constexpr int kWide = 2 * kBN;  // columns of a wide grad_H tile: 512
-template <int MODE>
-constexpr int stages2() { return MODE == kModeForward ? 6 : 4; }
-template <int MODE>
-constexpr int stage2_bytes() { return (MODE == kModeForward ? 2 : 3) * kHalf * kBK * 2; }
-template <int MODE>
-constexpr int gemm2_smem_bytes() { return stages2<MODE>() * stage2_bytes<MODE>() + 1024 + 1024; }
+constexpr int kRingSlots = 6;
+constexpr int kNarrowStageBytes = 2 * kHalf * kBK * 2;
+constexpr int kWideStages = 4;
+constexpr int kWideStageBytes = 3 * kHalf * kBK * 2;
+static_assert(kWideStages * kWideStageBytes <= kRingSlots * kNarrowStageBytes, "wide layout exceeds the ring");
+constexpr int kGemm2SmemBytes = kRingSlots * kNarrowStageBytes + 1024 + 1024;
 constexpr int kRingConsumers2 = 1 + kEpiWarps + 1 + kEpiWarps;  // leader MMA + epi, peer producer + epi
 constexpr int kHGroup = 8;  // row tiles per group in the grad_H tile order
 constexpr int kFGroup = 16;  // row tiles per group in the forward tile order
@@ -245,12 +247,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  constexpr int kStages2 = stages2<MODE>();
-  constexpr int kStage2Bytes = stage2_bytes<MODE>();
-  uint8_t* bar_area = smem_raw + (base - raw) + kStages2 * kStage2Bytes;
+  uint8_t* bar_area = smem_raw + (base - raw) + kRingSlots * kNarrowStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
-  uint64_t* empty = full + kStages2;
-  uint64_t* tfull = empty + kStages2;
+  uint64_t* empty = full + kRingSlots;
+  uint64_t* tfull = empty + kRingSlots;
   uint64_t* tempty = tfull + 2;
   uint64_t* ring_full = tempty + 2;
   uint64_t* ring_empty = ring_full + kTileRing;
@@ -265,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages2; ++s) {
+    for (int s = 0; s < kRingSlots; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
       mbar_init(smem_addr(&empty[s]), 1);
     }
@@ -300,8 +300,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_keep = l2_policy_evict_last();
       const uint64_t pol_stream = l2_policy_evict_first();
       int stage = 0, slot = 0;
-      uint32_t phase = 0, rphase = 0;
-      uint64_t issued = 0;
+      uint32_t rphase = 0;
+      uint32_t fills = 0;  // bit s: parity of the number of fills of stage s
+      bool wide = false;   // ring layout in use
       bool ok = true;
       while (ok) {
         int t;
@@ -332,12 +333,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const Tile2 ti = decode_tile2(MODE, t, p);
         const int mh = ti.m0 + kHalf * static_cast<int>(rank);  // this CTA's rows of A
         const int nh = ti.n0 + kHalf * static_cast<int>(rank);  // this CTA's columns of B
+        if ((ti.kind == 1) != wide) {
+          // the other layout's stages overlap these: wait until the MMAs have
+          // released every stage (the latest fill of each)
+          for (int s2 = 0; s2 < kRingSlots && ok; ++s2)
+            ok = mbar_wait_cluster(smem_addr(&empty[s2]), ((fills >> s2) & 1u) ^ 1u, ctl);
+          if (!ok) break;
+          wide = ti.kind == 1;
+          stage = 0;
+        }
+        const int nst = wide ? kWideStages : kRingSlots;
+        const uint32_t sbytes = wide ? kWideStageBytes : kNarrowStageBytes;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          if (!mbar_wait_cluster(smem_addr(&empty[stage]), phase ^ 1u, ctl)) {
+          if (!mbar_wait_cluster(smem_addr(&empty[stage]), ((fills >> stage) & 1u) ^ 1u, ctl)) {
             ok = false;
             break;
           }
-          const uint32_t sa = base + stage * kStage2Bytes;
+          const uint32_t sa = base + stage * sbytes;
           const uint32_t sb = sa + kHalf * kBK * 2;
           const uint32_t fb = map_to_cta(smem_addr(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), ti.kind == 1 ? 6 * kBoxBytes * 2 : 4 * kBoxBytes * 2);
@@ -368,28 +380,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tma_load_2d_pair_hint(sb, &tm_h, fb, nh, r, pol_keep);
             tma_load_2d_pair_hint(sb + kBoxBytes, &tm_h, fb, nh + 64, r, pol_keep);
           }
-          ++issued;
-          if (++stage == kStages2) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          fills ^= 1u << stage;
+          if (++stage == nst) stage = 0;
         }
       }
       if (!ok && leader) {
-        // Drain: copies still in flight must land before the pair exits.
-        for (int s = 0; s < kStages2; ++s) {
-          if (issued > static_cast<uint64_t>(s)) {
-            const uint64_t uses = (issued - 1 - s) / kStages2 + 1;
-            mbar_wait_cluster_drain(smem_addr(&full[s]), static_cast<uint32_t>((uses - 1) & 1u), p.timeout_ns);
-          }
-        }
+        // Drain: copies still in flight must land before the pair exits (the
+        // latest fill of each stage; a stage never filled passes at once).
+        for (int s2 = 0; s2 < kRingSlots; ++s2)
+          mbar_wait_cluster_drain(smem_addr(&full[s2]), ((fills >> s2) & 1u) ^ 1u, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && leader) {
       int stage = 0, slot = 0, acc = 0;
-      uint32_t phase = 0, rphase = 0, aphase = 0;
+      uint32_t rphase = 0, aphase = 0;
+      uint32_t uses = 0;  // bit s: parity of the number of times stage s was consumed
+      bool wide = false;
       for (;;) {
         if (!mbar_wait(smem_addr(&ring_full[slot]), rphase, ctl)) break;
         const int t = ring[slot];
@@ -417,6 +425,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (!got) break;
+        if ((ti.kind == 1) != wide) {  // same layout switch as the producer
+          wide = ti.kind == 1;
+          stage = 0;
+        }
+        const int nst = wide ? kWideStages : kRingSlots;
+        const uint32_t sbytes = wide ? kWideStageBytes : kNarrowStageBytes;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(bufs[0] * kBN);
         const uint32_t d_tmem1 = tmem_base + static_cast<uint32_t>(bufs[1] * kBN);
@@ -425,12 +439,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                               : instr_desc_bf16(256, kBN, 1, 1);
         bool aborted = false;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          if (!mbar_wait_cluster(smem_addr(&full[stage]), phase, ctl)) {
+          if (!mbar_wait_cluster(smem_addr(&full[stage]), (uses >> stage) & 1u, ctl)) {
             aborted = true;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sa = base + stage * kStage2Bytes;
+          const uint32_t sa = base + stage * sbytes;
           const uint32_t sb = sa + kHalf * kBK * 2;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
@@ -438,16 +452,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                              : smem_desc(sa + k * 32, 16, 1024);
             const uint64_t bd = ti.kind == 0 ? smem_desc(sb + k * 32, 16, 1024)
                                              : smem_desc(sb + k * 2048, 8192, 1024);
-            mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-            if (ti.kind == 1)  // second half of a wide tile: same A, the next two B boxes
-              mma_bf16_pair(d_tmem1, ad, smem_desc(sb + 2 * kBoxBytes + k * 2048, 8192, 1024), idesc,
-                            (kb | k) != 0 ? 1u : 0u);
+            if (ti.kind == 1) {  // wide tile: the two 256-column halves share A
+              mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_pair(
+                  d_tmem1, ad, smem_desc(sb + 2 * kBoxBytes + k * 2048, 8192, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
+            } else {
+              mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           mma_commit_pair(smem_addr(&empty[stage]), 0x3);
-          if (++stage == kStages2) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          uses ^= 1u << stage;
+          if (++stage == nst) stage = 0;
         }
         if (aborted) break;
         for (int q = 0; q < nbuf; ++q) mma_commit_pair(smem_addr(&tfull[bufs[q]]), 0x3);
@@ -517,10 +532,10 @@ int gemm2_max_smem_ok() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (configured[dev]) return 1;
   if (cudaFuncSetAttribute(gemm2_kernel<kModeForward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           gemm2_smem_bytes<kModeForward>()) != cudaSuccess)
+                           kGemm2SmemBytes) != cudaSuccess)
     return 0;
   if (cudaFuncSetAttribute(gemm2_kernel<kModeBackward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           gemm2_smem_bytes<kModeBackward>()) != cudaSuccess)
+                           kGemm2SmemBytes) != cudaSuccess)
     return 0;
   configured[dev] = 1;
   return 1;
@@ -532,9 +547,9 @@ cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& t
   if (!gemm2_max_smem_ok()) return cudaErrorInvalidConfiguration;
   prof_begin(s, mode == kModeForward ? FLCE_KERNEL_GEMM_FWD : FLCE_KERNEL_GEMM_BWD);
   if (mode == kModeForward)
-    gemm2_kernel<kModeForward><<<grid, kGemmThreads, gemm2_smem_bytes<kModeForward>(), s>>>(tm_h, tm_w, tm_z, p);
+    gemm2_kernel<kModeForward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
   else
-    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, gemm2_smem_bytes<kModeBackward>(), s>>>(tm_h, tm_w, tm_z, p);
+    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;
