@@ -223,6 +223,24 @@ class Step:
         self.ce_call()
 
 
+def peak_allocated_delta(step):
+    """Peak device memory one flce_fwd_bwd call adds over its inputs and
+    outputs (torch's peak-allocated counter around a fresh workspace and the
+    call): the library allocates nothing, so this is the workspace."""
+    import torch
+    torch.cuda.synchronize()
+    keep = step.ws
+    step.ws = None
+    del keep
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    step.ws = torch.empty(step.ws_bytes, dtype=torch.uint8, device=step.loss.device)
+    step.flce_call()
+    torch.cuda.synchronize()
+    return torch.cuda.max_memory_allocated() - base
+
+
 # --------------------------------------------------------------------- timing
 def timed_steps(step, steps, warmup, barrier):
     import torch
@@ -436,6 +454,7 @@ def main():
     step = Step(dev, device, args.chunk)
     if args.only_flce:
         step.ce_call = lambda: None
+    peak_delta = peak_allocated_delta(step)
     peaks, peak_src = load_peaks()
 
     # launches per step, from one recorded step
@@ -541,8 +560,8 @@ def main():
                              "kernel_frac": round(ce_kernel_gbs / peaks.get("hbm_gbs", 6800.0), 4),
                              "l2": "emptied before every call (256 MB written, then 256 MB read)", "scope": "gbs/frac: whole ce_fwd_bwd call "
                              "(count + ce_rows kernels); kernel_*: ce_rows alone", "clocks": ce_clocks},
-            "scratch": {"workspace_bytes": step.ws_bytes, "full_logits_bytes": n * v * 2,
-                        "chunk": chunk, "chunks": n_chunks},
+            "scratch": {"workspace_bytes": step.ws_bytes, "peak_allocated_delta_bytes": peak_delta,
+                        "full_logits_bytes": n * v * 2, "chunk": chunk, "chunks": n_chunks},
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "kernels": kernels, "clocks": clock_info, "status": status, "cpu_baseline": cpu,
         }
