@@ -366,6 +366,9 @@ def cpu_baseline(inp, rows=512):
                       f"(H={WORKLOAD['h']}, V={WORKLOAD['v']}, full grad_weight), {secs:.2f} s"}
 
 
+METRIC = "FLCE fwd+bwd tokens/s (+ % bf16 tensor peak; CE GB/s vs HBM; peak scratch)"
+
+
 def workload_config(chunk=None):
     w = WORKLOAD
     cfg = {"workload": f"FLCE fwd+bwd, Llama-3-8B lm_head: N={w['n']} (batch 4 x seq 4096), H={w['h']}, "
@@ -378,7 +381,8 @@ def workload_config(chunk=None):
 
 
 def variant_name(v):
-    return {1: "single-CTA 128x256 tiles", 2: "CTA-pair 256x256 tiles (cta_group::2)"}.get(v, str(v))
+    return {1: "single-CTA 128x256 tiles",
+            2: "CTA-pair tiles (cta_group::2): 256x256, grad_H 256x512"}.get(v, str(v))
 
 
 def run_reference(args):
@@ -387,18 +391,24 @@ def run_reference(args):
         return 0
     import synthetic_inputs as si
     inp = si.config_inputs(WORKLOAD["name"])
-    rows = args.ref_rows
-    for _ in range(args.warmup_ref):
+    # each step a bounded sample: the first `rows` tokens of the workload, sized
+    # so that warm-up + timed steps stay within a few minutes on the host
+    rows = args.ref_rows if args.ref_rows > 0 else max(16, min(256, (256 * 25) // (args.steps + args.warmup)))
+    for _ in range(args.warmup):
         oracle_sample(inp, rows)
-    times = [oracle_sample(inp, rows) for _ in range(max(1, args.steps_ref))]
+    times = [oracle_sample(inp, rows) for _ in range(args.steps)]
     secs = statistics.mean(times)
     value = rows / secs
-    line = {"impl": "reference", "metric": "FLCE fwd+bwd tokens/s", "value": value, "unit": "tokens/s",
-            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup_ref,
+    import linear_cross_entropy_03_gb300 as flce
+    w = WORKLOAD
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic", "config": workload_config(),
+            "dtype": "f64", "data": "synthetic",
+            "config": workload_config(flce.flce_default_chunk(w["n"], w["h"], w["v"])),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
-                             "sample": f"fp64 numpy oracle on the first {rows} tokens per step"},
+                             "sample": f"fp64 numpy oracle, fwd+bwd of the first {rows} of {w['n']} tokens per step "
+                                       f"(full H, V and grad_weight)"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -414,9 +424,7 @@ def main():
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256)
-    ap.add_argument("--ref-rows", type=int, default=256)
-    ap.add_argument("--steps-ref", type=int, default=3)
-    ap.add_argument("--warmup-ref", type=int, default=1)
+    ap.add_argument("--ref-rows", type=int, default=0, help="tokens per reference step (0: sized from K and W)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling runs only: use the first N tokens of the workload")
@@ -544,7 +552,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": "FLCE fwd+bwd tokens/s (+ % bf16 tensor peak; CE GB/s vs HBM; peak scratch)",
+            "metric": METRIC,
             "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
