@@ -149,6 +149,34 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
                            float* target_logit_out, void* workspace, size_t workspace_bytes,
                            int32_t* status_dev, flce_stream_t stream);
 
+/*
+ * flce_fwd_bwd_typed -- flce_fwd_bwd with the operand type given: dtype is
+ * FLCE_DTYPE_BF16 (exactly flce_fwd_bwd) or FLCE_DTYPE_FP16, for which
+ * hidden, weight, bias and grad_hidden are IEEE half (fp16) and everything
+ * else is as in flce_fwd_bwd, same workspace size.  Other dtypes return
+ * FLCE_ERR_UNSUPPORTED, and so does fp16 while the one-CTA GEMM form is
+ * selected (flce_set_gemm_variant).  The logits dtypes FP32 / FP16 / BF16 the
+ * DeepSpeed PR #8540 description ("optional Liger vocab-parallel CE
+ * backend", section "Changes") validates carry over to the fused form for
+ * the two 16-bit types.
+ *
+ * Arithmetic with fp16: fp16 x fp16 on the tensor cores with fp32
+ * accumulation; the chunk logits are kept in fp16, and the chunk's
+ * grad-logits are stored in fp16 divided by the part of the gradient scale
+ * common to all rows (g / n_valid for MEAN, g for SUM, g * max|grad_out| for
+ * NONE), so they lie in [-1, 1] rather than underflowing fp16's range; the
+ * two backward products multiply that factor back in fp32.  grad_bias is
+ * summed from the fp32 grad-logits.
+ */
+flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weight, const void* bias,
+                                 const int64_t* target, int64_t N, int64_t H, int64_t V,
+                                 int64_t ignore_index, int reduction, int64_t chunk,
+                                 float grad_scale, const float* grad_out_none, float* loss,
+                                 void* grad_hidden, float* grad_weight, float* grad_bias,
+                                 int accumulate, int32_t* n_valid_out, float* lse_out,
+                                 float* target_logit_out, void* workspace, size_t workspace_bytes,
+                                 int32_t* status_dev, flce_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Cross entropy on materialised logits
  * ------------------------------------------------------------------------ */

@@ -17,7 +17,7 @@ from typing import Optional
 __all__ = [
     "REDUCTIONS", "DTYPES", "STATUS_BIT_TARGET_RANGE", "STATUS_BIT_TIMEOUT", "KERNEL_NAMES",
     "library_path", "lib", "flce_status_string", "flce_version", "flce_default_chunk",
-    "flce_workspace_size", "flce_fwd_bwd", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
+    "flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_typed", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
     "flce_vp_workspace_size", "flce_vp_forward", "flce_vp_backward", "ce_vp_partials", "ce_vp_backward",
     "flce_set_gemm_variant", "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
     "flce_profile_enable", "flce_profile_disable", "flce_profile_read",
@@ -46,6 +46,9 @@ _SIGNATURES = {
     "flce_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_int, _I64,
                                     ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P,
                                     _P, _SZ, _P, _P]),
+    "flce_fwd_bwd_typed": (ctypes.c_int, [ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_int,
+                                          _I64, ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P,
+                                          _P, _SZ, _P, _P]),
     "ce_workspace_size": (_SZ, [_I64, _I64, ctypes.c_int, ctypes.c_int]),
     "ce_fwd_bwd": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                   ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
@@ -143,6 +146,16 @@ def flce_fwd_bwd(hidden, weight, bias, target, N, H, V, ignore_index, reduction,
         chunk, float(grad_scale), _ptr(grad_out_none), _ptr(loss), _ptr(grad_hidden), _ptr(grad_weight),
         _ptr(grad_bias), int(accumulate), _ptr(n_valid_out), _ptr(lse_out), _ptr(target_logit_out),
         _ptr(workspace), int(workspace_bytes), _ptr(status_dev), _stream(stream))
+
+
+def flce_fwd_bwd_typed(dtype, hidden, weight, bias, target, N, H, V, ignore_index, reduction, chunk, grad_scale,
+                       grad_out_none, loss, grad_hidden, grad_weight, grad_bias, accumulate, n_valid_out,
+                       lse_out, target_logit_out, workspace, workspace_bytes, status_dev, stream=None) -> int:
+    return lib().flce_fwd_bwd_typed(
+        _dt(dtype), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(target), N, H, V, ignore_index,
+        _red(reduction), chunk, float(grad_scale), _ptr(grad_out_none), _ptr(loss), _ptr(grad_hidden),
+        _ptr(grad_weight), _ptr(grad_bias), int(accumulate), _ptr(n_valid_out), _ptr(lse_out),
+        _ptr(target_logit_out), _ptr(workspace), int(workspace_bytes), _ptr(status_dev), _stream(stream))
 
 
 def ce_workspace_size(N: int, V: int, dtype="bf16", reduction="mean") -> int:
@@ -263,9 +276,10 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
                                row_stats: bool = False, workspace=None, status=None, stream=None) -> dict:
     """Loss and gradients of cross_entropy(hidden @ weight.T + bias, target).
 
-    hidden [N, H] bf16, weight [V, H] bf16, bias [V] bf16 or None, target [N]
-    int64, all on one CUDA device and contiguous.  Returns a dict with
-    ``loss`` (fp32 [N] or []), ``grad_hidden`` (bf16 [N, H]), ``grad_weight``
+    hidden [N, H] and weight [V, H] bf16 or fp16 (both the same), bias [V] of
+    that type or None, target [N] int64, all on one CUDA device and
+    contiguous.  Returns a dict with ``loss`` (fp32 [N] or []),
+    ``grad_hidden`` ([N, H], the input type), ``grad_weight``
     (fp32 [V, H]), ``grad_bias`` (fp32 [V]), ``n_valid`` (int32 [1]) and, with
     ``row_stats``, ``lse`` and ``target_logit`` (fp32 [N]).  Asynchronous on
     ``stream`` (default: the current stream); ``status`` is the device
@@ -277,7 +291,10 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
     dev = hidden.device
     red = _red(reduction)
     loss = torch.empty(n if red == 0 else 1, dtype=torch.float32, device=dev)
-    gh = torch.empty(n, h, dtype=torch.bfloat16, device=dev) if grad_hidden else None
+    if hidden.dtype not in (torch.bfloat16, torch.float16) or weight.dtype != hidden.dtype:
+        raise FlceError(2, "fused_linear_cross_entropy: hidden and weight must both be bf16 or both fp16")
+    dtype = "fp16" if hidden.dtype == torch.float16 else "bf16"
+    gh = torch.empty(n, h, dtype=hidden.dtype, device=dev) if grad_hidden else None
     gw = grad_weight_out if grad_weight_out is not None else (
         torch.empty(v, h, dtype=torch.float32, device=dev) if grad_weight else None)
     gb = grad_bias_out if grad_bias_out is not None else (
@@ -292,10 +309,10 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-    st = flce_fwd_bwd(hidden, weight, bias, target, n, h, v, ignore_index, red, chunk, grad_scale,
-                      grad_out, loss, gh, gw, gb, accumulate, nv, lse, tl, workspace, ws_bytes,
-                      status, stream)
-    _check(st, "flce_fwd_bwd")
+    st = flce_fwd_bwd_typed(dtype, hidden, weight, bias, target, n, h, v, ignore_index, red, chunk, grad_scale,
+                            grad_out, loss, gh, gw, gb, accumulate, nv, lse, tl, workspace, ws_bytes,
+                            status, stream)
+    _check(st, "flce_fwd_bwd_typed")
     out = dict(loss=loss if red == 0 else loss[0], grad_hidden=gh, grad_weight=gw, grad_bias=gb,
                n_valid=nv, status=status, workspace=workspace)
     if row_stats:

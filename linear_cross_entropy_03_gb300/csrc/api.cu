@@ -60,14 +60,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Row-major bf16 matrix [rows, cols] with row pitch `pitch_elems`, read in
 // 64 x 64 boxes with the 128-byte swizzle; out-of-range elements read as 0.
-bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t pitch_elems) {
+bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t pitch_elems,
+              CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems * 2)};
   cuuint32_t box[2] = {64, 64};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  const CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -192,10 +193,26 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
                            int64_t chunk, float grad_scale, const float* grad_out_none, float* loss,
                            void* grad_hidden, float* grad_weight, float* grad_bias, int accumulate,
                            int32_t* n_valid_out, float* lse_out, float* target_logit_out, void* workspace,
-                           size_t workspace_bytes, int32_t* status_dev, flce_stream_t stream_) {
+                           size_t workspace_bytes, int32_t* status_dev, flce_stream_t stream) {
+  return flce_fwd_bwd_typed(FLCE_DTYPE_BF16, hidden, weight, bias, target, N, H, V, ignore_index, reduction, chunk,
+                            grad_scale, grad_out_none, loss, grad_hidden, grad_weight, grad_bias, accumulate,
+                            n_valid_out, lse_out, target_logit_out, workspace, workspace_bytes, status_dev, stream);
+}
+
+flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weight, const void* bias,
+                                 const int64_t* target, int64_t N, int64_t H, int64_t V, int64_t ignore_index,
+                                 int reduction, int64_t chunk, float grad_scale, const float* grad_out_none,
+                                 float* loss, void* grad_hidden, float* grad_weight, float* grad_bias,
+                                 int accumulate, int32_t* n_valid_out, float* lse_out, float* target_logit_out,
+                                 void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                 flce_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FlceLayout L;
   if (N < 0 || V < 1 || H < 1 || chunk < 0 || reduction < 0 || reduction > 2) return FLCE_ERR_INVALID_ARG;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16) return FLCE_ERR_UNSUPPORTED;
+  const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
+  const bool fp16 = dtype == FLCE_DTYPE_FP16;
+  if (fp16 && !pair) return FLCE_ERR_UNSUPPORTED;  // fp16 operands: the CTA-pair kernels only
   if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
   if (!flce_layout(N, H, V, chunk, reduction, &L)) return FLCE_ERR_INVALID_ARG;
   if (loss == nullptr || weight == nullptr) return FLCE_ERR_INVALID_ARG;
@@ -224,7 +241,7 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
   FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, hdr_bytes, stream));
   FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, n_valid_out,
                                      (grad_bias != nullptr && !accumulate) ? grad_bias : nullptr,
-                                     (grad_bias != nullptr && !accumulate) ? V : 0, stream));
+                                     (grad_bias != nullptr && !accumulate) ? V : 0, grad_out_none, stream));
   if (N == 0) {
     if (grad_weight != nullptr && !accumulate) FLCE_TRY_CUDA(launch_zero(grad_weight, V * H, stream));
     if (reduction != FLCE_REDUCTION_NONE)
@@ -233,14 +250,16 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
   }
 
   CUtensorMap tm_h, tm_w, tm_z;
-  if (!make_map(&tm_h, hidden, H, N, H) || !make_map(&tm_w, weight, H, V, H)) return FLCE_ERR_CUDA;
+  const CUtensorMapDataType mtype = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&tm_h, hidden, H, N, H, mtype) || !make_map(&tm_w, weight, H, V, H, mtype)) return FLCE_ERR_CUDA;
   const int sms = device_sm_count();
+  const float* gmax = (reduction == FLCE_REDUCTION_NONE && grad_out_none != nullptr) ? &hdr->gmax : nullptr;
   const bool want_grads = grad_hidden != nullptr || grad_weight != nullptr || grad_bias != nullptr;
 
   for (int64_t k = 0; k < L.num_chunks; ++k) {
     const int64_t row0 = k * L.chunk;
     const int c_len = static_cast<int>(std::min<int64_t>(L.chunk, N - row0));
-    if (!make_map(&tm_z, zbuf, V, c_len, L.vp)) return FLCE_ERR_CUDA;
+    if (!make_map(&tm_z, zbuf, V, c_len, L.vp, mtype)) return FLCE_ERR_CUDA;
 
     GemmParams g = {};
     g.row0 = row0;
@@ -261,8 +280,12 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
     g.gw_store = (k == 0 && !accumulate) ? 1 : 0;
     g.status = status;
     g.timeout_ns = timeout;
+    g.in_fp16 = fp16 ? 1 : 0;
+    g.n_valid = &hdr->n_valid;
+    g.gmax = gmax;
+    g.reduction = reduction;
+    g.grad_scale = grad_scale;
 
-    const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
     const int tile_m = pair ? 2 * kBM : kBM;
     g.f_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.num_tiles = static_cast<int>(g.f_num_m * L.nvt);
@@ -296,6 +319,8 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
     r.zbuf = zbuf;
     r.ldz = L.vp;
     r.grad_bias = grad_bias;
+    r.z_fp16 = fp16 ? 1 : 0;
+    r.gmax = gmax;
     FLCE_TRY_CUDA(launch_row_finalize(r, stream));
     if (!want_grads) continue;
     FLCE_TRY_CUDA(launch_grad_logits(r, stream));
@@ -355,10 +380,10 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
 
   if (N <= kCountSingleBlockMax) {
     // one block zeroes the header and counts; the CE kernel overlaps it (PDL)
-    FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 1, status, nullptr, nullptr, 0, stream));
+    FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 1, status, nullptr, nullptr, 0, nullptr, stream));
   } else {
     FLCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WorkspaceHeader) + 16, stream));
-    FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, stream));
+    FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, nullptr, stream));
   }
   if (N > 0) {
     const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned(logits, 16) &&

@@ -84,7 +84,7 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
 
   // The header (valid-target count, block ticket, status) must start at zero.
   if (cudaMemsetAsync(hdr, 0, kHeaderBytes, stream) != cudaSuccess) return FLCE_ERR_CUDA;
-  if (launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, stream) !=
+  if (launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, nullptr, stream) !=
       cudaSuccess)
     return FLCE_ERR_CUDA;
   if (N > 0) {

@@ -47,6 +47,14 @@ struct GemmParams {
   float4* partials;         // [c_len, nvt]: (max, sum exp(z - max), same over bf16(z), 0)
   int nvt;
   float* tgt_logit;         // [c_len]
+  // operands: 0 bf16, 1 fp16 (hidden, weight, bias, chunk logits, grad_hidden)
+  int in_fp16;
+  // fp16 only: dZ is stored divided by the uniform part of the row scale
+  // (see uniform_scale), which the backward epilogue multiplies back in
+  const int* n_valid;
+  const float* gmax;
+  int reduction;
+  float grad_scale;
   // backward epilogue
   uint16_t* grad_hidden;    // bf16 [N, H] or null
   float* grad_hidden_f32;   // fp32 [N, H] instead of grad_hidden (a shard's partial), or null
@@ -80,9 +88,11 @@ struct RowParams {
   float* tl_out;            // [N] or null
   int* status;
   // grad-logits pass
-  uint16_t* zbuf;
+  uint16_t* zbuf;           // chunk logits, bf16 or (z_fp16) fp16
   int64_t ldz;
   float* grad_bias;         // [V] or null
+  int z_fp16;
+  const float* gmax;        // fp16: max |grad_out| over valid rows (reduction none)
 };
 
 struct CeParams {
@@ -106,11 +116,27 @@ struct CeParams {
   int64_t v_offset;         // global id of this shard's first column
 };
 
+// fp16 operands: the part of every row's gradient scale that is the same for
+// all rows (mean: g / n_valid; sum: g; none: g * max |grad_out|, or g).  The
+// chunk's dZ is stored in fp16 divided by it, so its entries stay within
+// [-1, 1] instead of underflowing, and the backward products multiply it back.
+__device__ __forceinline__ float uniform_scale(int reduction, float grad_scale, const int* n_valid,
+                                              const float* gmax) {
+  if (reduction == FLCE_REDUCTION_MEAN) {
+    const int nv = *n_valid;
+    return nv > 0 ? grad_scale / static_cast<float>(nv) : 0.f;
+  }
+  if (reduction == FLCE_REDUCTION_SUM || gmax == nullptr) return grad_scale;
+  return grad_scale * *gmax;
+}
+
 // Header at the start of every workspace.
 struct WorkspaceHeader {
   int status;
   int n_valid;
   int pad[2];               // [0]: count kernel block ticket, [1]: CE kernel block ticket
+  float gmax;               // max |grad_out| over valid rows, when asked for
+  int pad2;
   double loss_sum;
   unsigned int tile_counters[];  // two per chunk
 };
@@ -121,10 +147,11 @@ struct WorkspaceHeader {
 // header's own, counts, tickets and `num_counters` tile counters) before
 // counting, so no memset is needed; otherwise the caller zeroes the header.
 constexpr int64_t kCountSingleBlockMax = 65536;
+// grad_out (optional): also leaves max |grad_out| over the valid rows in hdr->gmax.
 cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
                                  WorkspaceHeader* hdr, int num_counters, int zero_header,
                                  int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
-                                 cudaStream_t s);
+                                 const float* grad_out, cudaStream_t s);
 cudaError_t launch_gemm(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,
                         const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,

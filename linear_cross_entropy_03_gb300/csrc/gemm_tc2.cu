@@ -17,6 +17,7 @@
 //   warps 2-5 epilogue of this CTA's 128 accumulator rows
 // Operand bytes of both CTAs complete on the leader's stage barriers; the
 // leader's tcgen05.commit arrives on the matching barriers of both CTAs.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "ptx.cuh"
@@ -95,6 +96,26 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// 16-bit operand values: bf16, or fp16 when F16.  A packed pair holds the
+// element of the lower column in its low half.
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t w) {
+  return F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))) : bf16_lo(w);
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t w) {
+  return F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))) : bf16_hi(w);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if (F16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return pack_bf16x2(lo, hi);
+}
+
+template <bool F16>
 __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias, int lim) {
   if (lim >= 32) {
     const uint4* b4 = reinterpret_cast<const uint4*>(bias);
@@ -104,20 +125,23 @@ __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias,
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        x[8 * g + 2 * i] += bf16_lo(w[i]);
-        x[8 * g + 2 * i + 1] += bf16_hi(w[i]);
+        x[8 * g + 2 * i] += lo16<F16>(w[i]);
+        x[8 * g + 2 * i + 1] += hi16<F16>(w[i]);
       }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (j < lim) x[j] += __uint_as_float(static_cast<uint32_t>(__ldg(bias + j)) << 16);
+      if (j < lim) x[j] += lo16<F16>(static_cast<uint32_t>(__ldg(bias + j)));
   }
 }
 
 // Epilogue of one tile for this warp's 32 accumulator rows (`rl` = row
-// within the pair tile of this thread).
-__device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl) {
+// within the pair tile of this thread).  F16: fp16 operands (chunk logits and
+// grad_hidden in fp16); out_scale multiplies the backward products.
+template <bool F16>
+__device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl,
+                                              float out_scale) {
   if (ti.kind == 0) {
     const int r = ti.m0 + rl;
     const bool row_ok = r < p.c_len;
@@ -138,10 +162,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
       const int lim = ncols - c;
-      if (p.bias != nullptr) add_bias32(x, p.bias + ti.n0 + c, lim);
+      if (p.bias != nullptr) add_bias32<F16>(x, p.bias + ti.n0 + c, lim);
       uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+      for (int i = 0; i < 16; ++i) pk[i] = pack16<F16>(x[2 * i], x[2 * i + 1]);
       float cmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -154,11 +178,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
       for (int i = 0; i < 16; ++i) {
         if (2 * i < lim) {
           s32 += __expf(x[2 * i] - m_new);
-          s16 += __expf(bf16_lo(pk[i]) - m_new);
+          s16 += __expf(lo16<F16>(pk[i]) - m_new);
         }
         if (2 * i + 1 < lim) {
           s32 += __expf(x[2 * i + 1] - m_new);
-          s16 += __expf(bf16_hi(pk[i]) - m_new);
+          s16 += __expf(hi16<F16>(pk[i]) - m_new);
         }
       }
       m_run = m_new;
@@ -202,10 +226,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
         for (int g4 = 0; g4 < 4; ++g4)
           if (8 * g4 < lim)
             *reinterpret_cast<uint4*>(out + c + 8 * g4) = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * g4 + 0]), __uint_as_float(v[8 * g4 + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * g4 + 2]), __uint_as_float(v[8 * g4 + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * g4 + 4]), __uint_as_float(v[8 * g4 + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * g4 + 6]), __uint_as_float(v[8 * g4 + 7])));
+                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 0]), out_scale * __uint_as_float(v[8 * g4 + 1])),
+                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 2]), out_scale * __uint_as_float(v[8 * g4 + 3])),
+                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 4]), out_scale * __uint_as_float(v[8 * g4 + 5])),
+                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 6]), out_scale * __uint_as_float(v[8 * g4 + 7])));
       }
     }
   } else {
@@ -223,8 +247,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           if (c + 4 * g < ncols) {
-            float4 a = make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                   __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+            float4 a = make_float4(out_scale * __uint_as_float(v[4 * g]), out_scale * __uint_as_float(v[4 * g + 1]),
+                                   out_scale * __uint_as_float(v[4 * g + 2]), out_scale * __uint_as_float(v[4 * g + 3]));
             if (!p.gw_store) {  // read-add-write, streamed past L2's resident data
               const float4 b = __ldcs(o4 + g);
               a.x += b.x;
@@ -434,9 +458,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(bufs[0] * kBN);
         const uint32_t d_tmem1 = tmem_base + static_cast<uint32_t>(bufs[1] * kBN);
-        const uint32_t idesc = ti.kind == 0   ? instr_desc_bf16(256, kBN, 0, 0)
-                               : ti.kind == 1 ? instr_desc_bf16(256, kBN, 0, 1)
-                                              : instr_desc_bf16(256, kBN, 1, 1);
+        uint32_t idesc = ti.kind == 0   ? instr_desc_bf16(256, kBN, 0, 0)
+                         : ti.kind == 1 ? instr_desc_bf16(256, kBN, 0, 1)
+                                        : instr_desc_bf16(256, kBN, 1, 1);
+        if (p.in_fp16) idesc &= ~((7u << 7) | (7u << 10));  // A and B format fields: fp16 (0)
         bool aborted = false;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           if (!mbar_wait_cluster(smem_addr(&full[stage]), (uses >> stage) & 1u, ctl)) {
@@ -477,6 +502,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------ epilogue warps
     const int q = warp & 3;
+    // fp16: the chunk's dZ was stored divided by the rows' common scale
+    const float out_scale = (MODE == kModeBackward && p.in_fp16)
+                                ? uniform_scale(p.reduction, p.grad_scale, p.n_valid, p.gmax)
+                                : 1.f;
     const uint32_t leader_tempty0 = map_to_cta(smem_addr(&tempty[0]), 0);
     const uint32_t leader_tempty1 = map_to_cta(smem_addr(&tempty[1]), 0);
     int slot = 0, acc = 0;
@@ -503,7 +532,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after_sync();
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-        epilogue_tile(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane);
+        if (p.in_fp16)
+          epilogue_tile<true>(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane, out_scale);
+        else
+          epilogue_tile<false>(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane, 1.f);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);

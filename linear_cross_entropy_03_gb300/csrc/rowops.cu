@@ -25,13 +25,14 @@ constexpr int kCountThreads = 1024;
 __global__ void __launch_bounds__(kCountThreads)
     count_targets_kernel(const int64_t* __restrict__ target, int64_t N, int64_t V, int64_t ignore_index,
                          WorkspaceHeader* hdr, int* status, int32_t* n_valid_out, float* zero_a,
-                         int64_t zero_a_n, int zero_header, int num_counters) {
+                         int64_t zero_a_n, int zero_header, int num_counters, const float* grad_out) {
   grid_dependents_launch();
   if (zero_header) {  // single block: clear the header first
     if (threadIdx.x == 0) {
       if (status == &hdr->status) hdr->status = 0;
       hdr->pad[0] = 0;
       hdr->pad[1] = 0;
+      hdr->gmax = 0.f;
       hdr->loss_sum = 0.0;
     }
     for (int i = threadIdx.x; i < num_counters; i += blockDim.x) hdr->tile_counters[i] = 0u;
@@ -42,14 +43,22 @@ __global__ void __launch_bounds__(kCountThreads)
     zero_a[i] = 0.f;
   int cnt = 0;
   bool bad = false;
+  float gm = 0.f;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < N; i += stride) {
     const int64_t t = target[i];
     if (t != ignore_index) {
-      if (t >= 0 && t < V)
+      if (t >= 0 && t < V) {
         ++cnt;
-      else
+        if (grad_out != nullptr) gm = fmaxf(gm, fabsf(grad_out[i]));
+      } else {
         bad = true;
+      }
     }
+  }
+  if (grad_out != nullptr) {  // non-negative floats order like their bit patterns
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+    if ((threadIdx.x & 31) == 0 && gm > 0.f) atomicMax(reinterpret_cast<int*>(&hdr->gmax), __float_as_int(gm));
   }
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, FLCE_STATUS_BIT_TARGET_RANGE);
 #pragma unroll
@@ -135,6 +144,26 @@ constexpr int kGlCols = kGlThreads * 8;  // one 16-byte vector of bf16 per threa
 constexpr int kGlRows = 32;              // rows per block (bias column sums)
 constexpr int kGlUnroll = 4;
 
+// F16: fp16 chunk logits; dZ is stored divided by the rows' common scale
+// (uniform_scale), which the backward products multiply back in.
+template <bool F16>
+__device__ __forceinline__ float z_lo(uint32_t w) {
+  return F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))) : bf16_lo(w);
+}
+template <bool F16>
+__device__ __forceinline__ float z_hi(uint32_t w) {
+  return F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))) : bf16_hi(w);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t z_pack(float lo, float hi) {
+  if (F16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return pack_bf16x2(lo, hi);
+}
+
+template <bool F16>
 __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams p) {
   __shared__ float s_lse[kGlRows], s_scale[kGlRows];
   __shared__ int s_tgt[kGlRows];
@@ -156,6 +185,11 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
   const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kGlCols + threadIdx.x * 8;
   if (v0 >= p.V) return;
   const int nval = p.V - v0 < 8 ? static_cast<int>(p.V - v0) : 8;
+  float store_mul = 1.f;
+  if (F16) {
+    const float u = uniform_scale(p.reduction, p.grad_scale, p.n_valid, p.gmax);
+    store_mul = u != 0.f ? 1.f / u : 0.f;
+  }
   float cs[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) cs[j] = 0.f;
@@ -184,8 +218,8 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
       float d[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        d[2 * i] = bf16_lo(w[i]);
-        d[2 * i + 1] = bf16_hi(w[i]);
+        d[2 * i] = z_lo<F16>(w[i]);
+        d[2 * i + 1] = z_hi<F16>(w[i]);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -194,10 +228,10 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
         if (j < nval) cs[j] += d[j];
       }
       uint4 o;
-      o.x = pack_bf16x2(d[0], d[1]);
-      o.y = pack_bf16x2(d[2], d[3]);
-      o.z = pack_bf16x2(d[4], d[5]);
-      o.w = pack_bf16x2(d[6], d[7]);
+      o.x = z_pack<F16>(store_mul * d[0], store_mul * d[1]);
+      o.y = z_pack<F16>(store_mul * d[2], store_mul * d[3]);
+      o.z = z_pack<F16>(store_mul * d[4], store_mul * d[5]);
+      o.w = z_pack<F16>(store_mul * d[6], store_mul * d[7]);
       __stcs(dst, o);
     }
   }
@@ -347,14 +381,14 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaS
 cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, int64_t ignore_index,
                                  WorkspaceHeader* hdr, int num_counters, int zero_header,
                                  int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
-                                 cudaStream_t s) {
+                                 const float* grad_out, cudaStream_t s) {
   const int64_t work = N > zero_a_n ? N : zero_a_n;
   int blocks = static_cast<int>((work + kCountThreads * 4 - 1) / (kCountThreads * 4));
   blocks = blocks < 1 ? 1 : (blocks > sm_count() ? sm_count() : blocks);
   if (zero_header) blocks = 1;
   prof_begin(s, FLCE_KERNEL_COUNT_TARGETS);
   count_targets_kernel<<<blocks, kCountThreads, 0, s>>>(target, N, V, ignore_index, hdr, status, n_valid_out,
-                                                       zero_a, zero_a_n, zero_header, num_counters);
+                                                       zero_a, zero_a_n, zero_header, num_counters, grad_out);
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;
@@ -377,8 +411,9 @@ cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s) {
   prof_begin(s, FLCE_KERNEL_GRAD_LOGITS);
   RowParams pc = p;
   void* args[] = {&pc};
-  const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(grad_logits_kernel), grid,
-                                   dim3(kGlThreads), args, s, false);
+  const void* fn = p.z_fp16 ? reinterpret_cast<const void*>(grad_logits_kernel<true>)
+                            : reinterpret_cast<const void*>(grad_logits_kernel<false>);
+  const cudaError_t e = launch_pdl(fn, grid, dim3(kGlThreads), args, s, false);
   prof_end(s);
   return e;
 }

@@ -211,11 +211,11 @@ def ignore_positions(seed: int, stream: int, n: int, frac: float) -> np.ndarray:
 
 @dataclasses.dataclass
 class FlceInputs:
-    """One FLCE problem: bf16 bit patterns plus int64 targets."""
+    """One FLCE problem: bf16 bit patterns (uint16) or float16 values, plus int64 targets."""
 
-    hidden: np.ndarray            # uint16 [N, H] (bf16 bits)
-    weight: np.ndarray            # uint16 [V, H] (bf16 bits)
-    bias: Optional[np.ndarray]    # uint16 [V] (bf16 bits) or None
+    hidden: np.ndarray            # [N, H]: uint16 bf16 bits, or float16
+    weight: np.ndarray            # [V, H]: same type as hidden
+    bias: Optional[np.ndarray]    # [V]: same type, or None
     target: np.ndarray            # int64 [N]
     ignore_index: int = IGNORE_INDEX
 
@@ -232,10 +232,19 @@ def make_flce_inputs(n: int, h: int, v: int, seed: int, *, h_std: float = 1.0,
                      w_std: float = 0.02, bias_std: Optional[float] = None,
                      targets: str = "uniform", zipf_s: float = 1.1,
                      ignore_frac: float = 0.05,
-                     ignore_index: int = IGNORE_INDEX) -> FlceInputs:
-    hidden = normal_bf16(seed, _S_HIDDEN, (n, h), h_std)
-    weight = normal_bf16(seed, _S_WEIGHT, (v, h), w_std)
-    bias = normal_bf16(seed, _S_BIAS, (v,), bias_std) if bias_std is not None else None
+                     ignore_index: int = IGNORE_INDEX, dtype: str = "bf16") -> FlceInputs:
+    """dtype "bf16": bf16 bit patterns; "fp16": float16 values (float64 draw ->
+    float32 -> float16, round to nearest even)."""
+    if dtype == "bf16":
+        gen = normal_bf16
+    elif dtype == "fp16":
+        def gen(sd, st, shape, std):
+            return normal_f32(sd, st, shape, std).astype(np.float16)
+    else:
+        raise ValueError(dtype)
+    hidden = gen(seed, _S_HIDDEN, (n, h), h_std)
+    weight = gen(seed, _S_WEIGHT, (v, h), w_std)
+    bias = gen(seed, _S_BIAS, (v,), bias_std) if bias_std is not None else None
     if targets == "uniform":
         t = uniform_targets(seed, _S_TARGET, n, v)
     elif targets == "zipf":

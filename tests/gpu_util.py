@@ -21,6 +21,13 @@ def dev_bf16(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
+def dev16(a: np.ndarray) -> torch.Tensor:
+    """bf16 bit patterns (uint16) or float16 values on the GPU, as bf16 / fp16."""
+    if a.dtype == np.float16:
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return dev_bf16(a)
+
+
 def host(t) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
@@ -28,9 +35,9 @@ def host(t) -> np.ndarray:
 def run_flce(inp, *, reduction="mean", chunk=0, use_bias=True, grad_scale=1.0, grad_out=None,
              accumulate=False, grad_weight_init=None, grad_bias_init=None, ignore_index=None,
              grads=True, keep_f32=False):
-    h = dev_bf16(inp.hidden)
-    w = dev_bf16(inp.weight)
-    b = dev_bf16(inp.bias) if (use_bias and inp.bias is not None) else None
+    h = dev16(inp.hidden)
+    w = dev16(inp.weight)
+    b = dev16(inp.bias) if (use_bias and inp.bias is not None) else None
     t = torch.from_numpy(inp.target).cuda()
     go = torch.from_numpy(grad_out).cuda() if grad_out is not None else None
     gw0 = torch.from_numpy(grad_weight_init.astype(np.float32)).cuda() if grad_weight_init is not None else None

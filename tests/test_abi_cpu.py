@@ -66,6 +66,17 @@ def test_flce_rejects_bad_arguments(lib, kw, code):
     assert _flce(**kw) == code
 
 
+def test_flce_typed_rejects_other_dtypes(lib):
+    base = dict(hidden=FAKE, weight=FAKE, bias=None, target=FAKE, N=16, H=64, V=100, ignore_index=-100,
+                reduction=2, chunk=0, grad_scale=1.0, grad_out_none=None, loss=FAKE, grad_hidden=None,
+                grad_weight=None, grad_bias=None, accumulate=0, n_valid_out=None, lse_out=None,
+                target_logit_out=None, workspace=FAKE, workspace_bytes=1 << 40, status_dev=None, stream=0)
+    assert flce.flce_fwd_bwd_typed("fp32", **base) == 2
+    assert flce.flce_fwd_bwd_typed(7, **base) == 2
+    assert flce.flce_fwd_bwd_typed("fp16", **dict(base, N=-1)) == 1
+    assert flce.flce_fwd_bwd_typed("fp16", **dict(base, hidden=FAKE + 8)) == 7
+
+
 def _ce(**kw):
     args = dict(logits=FAKE, dtype=0, grad_logits=FAKE, target=FAKE, N=16, V=100, ignore_index=-100,
                 reduction=2, grad_scale=1.0, grad_out_none=None, loss=FAKE, workspace=FAKE,
