@@ -343,6 +343,140 @@ def e2e_steps(step, host, dev, steps, warmup, barrier):
     return t0.elapsed_time(t1), h2d, d2h
 
 
+def _device_ms(fn, steps, warmup):
+    """Mean device time of fn() over `steps` calls after `warmup` (CUDA events)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def next_rows(step, steps=5, warmup=3):
+    """The widened rows on the same shapes, fewer steps: forward-only FLCE,
+    FLCE with fp16 operands, FLCE on one vocabulary shard of two (forward
+    partials + backward from given row statistics, every chunk), CE on fp16 /
+    fp32 logits, CE on two vocabulary shards (partials + backward)."""
+    import torch
+    flce = step.flce
+    d = step.dev
+    n, h, v, chunk = step.n, step.h, step.v, step.chunk
+    dev = step.loss.device
+    peak_tf = load_peaks()[0].get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    hbm = load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out = {}
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {flce.flce_status_string(st)}")
+
+    # forward only (loss, no gradients): 2 N H V FLOPs
+    def fwd_only():
+        check(flce.flce_fwd_bwd(d["hidden"], d["weight"], None, d["target"], n, h, v, -100, step.red, chunk, 1.0,
+                                None, step.loss, None, None, None, 0, None, None, None, step.ws, step.ws_bytes,
+                                step.status, step.stream), "forward-only")
+    ms = _device_ms(fwd_only, steps, warmup)
+    tf = 2.0 * n * h * v / (ms / 1e3) / 1e12
+    out["flce_forward_only"] = {"tokens_per_s": round(n / (ms / 1e3), 1), "ms": round(ms, 3),
+                                "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak_tf, 4)}
+
+    # fp16 hidden / weight, full forward + backward (fp16 tensor rate = bf16's)
+    h16, w16 = d["hidden"].half(), d["weight"].half()
+    gh16 = torch.empty(n, h, dtype=torch.float16, device=dev)
+
+    def fp16_step():
+        check(flce.flce_fwd_bwd_typed("fp16", h16, w16, None, d["target"], n, h, v, -100, step.red, chunk, 1.0,
+                                      None, step.loss, gh16, step.grad_weight, None, 0, None, None, None, step.ws,
+                                      step.ws_bytes, step.status, step.stream), "fp16")
+    ms = _device_ms(fp16_step, steps, warmup)
+    tf = 6.0 * n * h * v / (ms / 1e3) / 1e12
+    out["flce_fp16"] = {"tokens_per_s": round(n / (ms / 1e3), 1), "ms": round(ms, 3), "tflops": round(tf, 1),
+                        "frac_of_bf16_peak": round(tf / peak_tf, 4)}
+    del h16, w16, gh16
+
+    # one vocabulary shard of two: per chunk, the shard's forward partials, then
+    # its backward from row statistics (here the shard's own; the combine is the caller's)
+    vs = v // 2
+    w_sh = d["weight"][:vs]
+    c = chunk
+    vp_ws_bytes = flce.flce_vp_workspace_size(c, h, vs)
+    vp_ws = torch.empty(vp_ws_bytes, dtype=torch.uint8, device=dev)
+    lse, lse16, zt = (torch.empty(c, device=dev) for _ in range(3))
+    scale = torch.full((c,), 1.0 / n, device=dev)
+    gh32 = torch.empty(c, h, device=dev)
+    gw_sh = step.grad_weight[:vs]
+
+    def vp_step():
+        for k, r0 in enumerate(range(0, n, c)):
+            cl = min(c, n - r0)
+            hid, tgt = d["hidden"][r0:r0 + cl], d["target"][r0:r0 + cl]
+            check(flce.flce_vp_forward(hid, w_sh, None, tgt, cl, h, vs, 0, -100, lse, lse16, zt, vp_ws,
+                                       vp_ws_bytes, step.status, step.stream), "vp forward")
+            check(flce.flce_vp_backward(hid, w_sh, tgt, cl, h, vs, 0, -100, lse16, scale, gh32, gw_sh, None,
+                                        1 if k else 0, vp_ws, vp_ws_bytes, step.status, step.stream), "vp backward")
+    ms = _device_ms(vp_step, steps, warmup)
+    tf = 6.0 * n * h * vs / (ms / 1e3) / 1e12
+    out["vp_flce_shard_of_2"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak_tf, 4),
+                                 "tokens_per_s_two_ranks": round(n / (ms / 1e3), 1)}
+    del vp_ws, gh32
+
+    # CE on fp16 / fp32 logits and on two vocabulary shards (L2 emptied before each call)
+    cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    tgt = d["ce_target"]
+    ws = torch.empty(flce.ce_workspace_size(cn, cv, "fp32", "mean"), dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, device=dev)
+
+    def ce_ms(call, iters=20):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for i in range(iters + 3):
+            flush.fill_(i & 0xFF)
+            clean.sum()
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(a.elapsed_time(b))
+        return statistics.median(times)
+
+    for name, tdt, b in (("fp16", torch.float16, 2), ("fp32", torch.float32, 4)):
+        z = d["logits"].to(tdt)
+        ms = ce_ms(lambda: check(flce.ce_fwd_bwd(z, name, z, tgt, cn, cv, -100, "mean", 1.0, None, loss, ws,
+                                                 ws.numel(), step.status, step.stream), "ce " + name))
+        gbs = (2 * cn * cv * b + 12 * cn) / (ms / 1e3) / 1e9
+        out[f"ce_logits_{name}"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+        del z
+    half = cv // 2
+    shards = [d["logits"][:, :half].contiguous(), d["logits"][:, half:].contiguous()]
+    slse = [torch.empty(cn, device=dev) for _ in shards]
+    szt = [torch.empty(cn, device=dev) for _ in shards]
+    comb = torch.empty(cn, device=dev)
+    rs = torch.full((cn,), 1.0 / cn, device=dev)
+
+    def ce_vp():
+        for k, zs in enumerate(shards):
+            check(flce.ce_vp_partials(zs, "bf16", tgt, cn, half, k * half, -100, slse[k], szt[k], step.status,
+                                      step.stream), "ce vp partials")
+        torch.logaddexp(slse[0], slse[1], out=comb)  # the cross-shard combine (the caller's all-reduce)
+        for k, zs in enumerate(shards):
+            check(flce.ce_vp_backward(zs, "bf16", zs, tgt, cn, half, k * half, -100, comb, rs, step.status,
+                                      step.stream), "ce vp backward")
+    ms = ce_ms(ce_vp)
+    gbs = (2 * cn * cv * 2 + 12 * cn) / (ms / 1e3) / 1e9
+    out["ce_vp_two_shards"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                               "note": "two passes over each shard (partials, then gradient) plus the combine"}
+    return out
+
+
 def aggregate_tokens_per_s(ms_local, tokens_per_rank, world, all_reduce_max):
     """Whole-job throughput: every rank's tokens over the slowest rank's time."""
     ms = all_reduce_max(ms_local)
@@ -426,6 +560,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256)
     ap.add_argument("--ref-rows", type=int, default=0, help="tokens per reference step (0: sized from K and W)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the widened rows' measurements")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling runs only: use the first N tokens of the workload")
     ap.add_argument("--only-flce", action="store_true", help="profiling runs only: skip the CE leg")
@@ -546,6 +681,8 @@ def main():
         e2e = {"value": n * ws / (float(te.item()) / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(float(te.item()), 3)}
 
+    widened = next_rows(step) if (rank == 0 and not args.only_flce and not args.no_next) else None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, args.cpu_rows)
@@ -570,6 +707,7 @@ def main():
                              "(count + ce_rows kernels); kernel_*: ce_rows alone", "clocks": ce_clocks},
             "scratch": {"workspace_bytes": step.ws_bytes, "peak_allocated_delta_bytes": peak_delta,
                         "full_logits_bytes": n * v * 2, "chunk": chunk, "chunks": n_chunks},
+            "next_rows": widened,
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "kernels": kernels, "clocks": clock_info, "status": status, "cpu_baseline": cpu,
         }
