@@ -357,13 +357,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <typename T>
 __device__ __forceinline__ float vec_max(const uint4& v);
 template <>
-__device__ __forceinline__ float vec_max<__half>(const uint4& v) {
-  __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y));
-  const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w));
-  a = __hmax2(a, b);
-  return fmaxf(__low2float(a), __high2float(a));
-}
-template <>
 __device__ __forceinline__ float vec_max<float>(const uint4& v) {
   return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
 }
@@ -406,6 +399,35 @@ __device__ __forceinline__ float vec_max_all<uint16_t, 8>(const uint4 (&v)[8], i
 template <>
 __device__ __forceinline__ float vec_max_all<uint16_t, 10>(const uint4 (&v)[10], int limit, int step) {
   return vec_max_all_bf16<10>(v, limit, step);
+}
+// fp16: the same running packed maximum in half2
+template <int VPT>
+__device__ __forceinline__ float vec_max_all_f16(const uint4 (&v)[VPT], int limit, int step) {
+  __half2 m = __float2half2_rn(-INFINITY);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    if (i * step < limit) {
+      const __half2* w = reinterpret_cast<const __half2*>(&v[i]);
+      m = __hmax2(m, __hmax2(__hmax2(w[0], w[1]), __hmax2(w[2], w[3])));
+    }
+  }
+  return fmaxf(__low2float(m), __high2float(m));
+}
+template <>
+__device__ __forceinline__ float vec_max_all<__half, 2>(const uint4 (&v)[2], int limit, int step) {
+  return vec_max_all_f16<2>(v, limit, step);
+}
+template <>
+__device__ __forceinline__ float vec_max_all<__half, 4>(const uint4 (&v)[4], int limit, int step) {
+  return vec_max_all_f16<4>(v, limit, step);
+}
+template <>
+__device__ __forceinline__ float vec_max_all<__half, 8>(const uint4 (&v)[8], int limit, int step) {
+  return vec_max_all_f16<8>(v, limit, step);
+}
+template <>
+__device__ __forceinline__ float vec_max_all<__half, 10>(const uint4 (&v)[10], int limit, int step) {
+  return vec_max_all_f16<10>(v, limit, step);
 }
 
 // Replaces every element z by exp(z - m) and adds the exponentials into the

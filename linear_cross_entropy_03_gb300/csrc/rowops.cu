@@ -307,6 +307,38 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same with 16-byte vectors (rows of a multiple of 16 bytes, 16-byte
+// aligned): one vector per thread and step, grid (vectors of a row, rows).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    ce_vp_grad_vec_kernel(const T* __restrict__ logits, T* grad, const int64_t* __restrict__ target, int64_t N,
+                          int64_t V, int64_t v_offset, int64_t ignore_index, const float* __restrict__ lse,
+                          const float* __restrict__ row_scale) {
+  constexpr int EPV = 16 / sizeof(T);
+  const int64_t nvec = V / EPV;
+  for (int64_t row = blockIdx.y; row < N; row += gridDim.y) {
+    const int64_t tg = target[row];
+    const int64_t tl = tg - v_offset;
+    const int64_t t = (tg != ignore_index && tl >= 0 && tl < V) ? tl : -1;
+    const float sc = row_scale[row];
+    const float l = lse[row];
+    const uint4* x = reinterpret_cast<const uint4*>(logits + row * V);
+    uint4* g = reinterpret_cast<uint4*>(grad + row * V);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      uint4 u = sc == 0.f ? make_uint4(0, 0, 0, 0) : __ldcs(x + i);
+      T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+      for (int k = 0; k < EPV; ++k) {
+        const int64_t v = i * EPV + k;
+        const float d = sc == 0.f ? 0.f : sc * (__expf(load_as_f(e + k) - l) - (v == t ? 1.f : 0.f));
+        store_f(e + k, d);
+      }
+      __stcs(g + i, u);
+    }
+  }
+}
+
 constexpr int kReduceThreads = 1024;
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -432,6 +464,30 @@ cudaError_t launch_ce_vp_grad(const void* logits, void* grad, int dtype, const i
                               int64_t V, int64_t v_offset, int64_t ignore_index, const float* lse,
                               const float* row_scale, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
+  const size_t esz = dtype == FLCE_DTYPE_FP32 ? 4 : 2;
+  const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(logits) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(grad) % 16 == 0;
+  if (vec) {
+    const int64_t nvec = static_cast<int64_t>(V) * esz / 16;
+    int64_t bx = (nvec + 255) / 256;
+    if (bx > 64) bx = 64;
+    const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(N < 65535 ? N : 65535));
+    prof_begin(s, FLCE_KERNEL_CE_ROWS);
+    if (dtype == FLCE_DTYPE_BF16)
+      ce_vp_grad_vec_kernel<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(logits),
+                                                            static_cast<uint16_t*>(grad), target, N, V, v_offset,
+                                                            ignore_index, lse, row_scale);
+    else if (dtype == FLCE_DTYPE_FP16)
+      ce_vp_grad_vec_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(logits),
+                                                          static_cast<__half*>(grad), target, N, V, v_offset,
+                                                          ignore_index, lse, row_scale);
+    else
+      ce_vp_grad_vec_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(logits), static_cast<float*>(grad),
+                                                         target, N, V, v_offset, ignore_index, lse, row_scale);
+    const cudaError_t e = cudaGetLastError();
+    prof_end(s);
+    return e;
+  }
   int64_t bx = (V + 255) / 256;
   if (bx > 64) bx = 64;
   const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(N < 65535 ? N : 65535));
