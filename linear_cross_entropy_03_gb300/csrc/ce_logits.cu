@@ -485,14 +485,14 @@ __device__ __forceinline__ void vec_scale<uint16_t>(uint4& v, float factor) {
 }
 template <>
 __device__ __forceinline__ void vec_scale<__half>(uint4& v, float factor) {
-  // fp16's range cannot hold small factors: multiply in fp32
+  // packed fp16 multiplies; a factor below fp16's normal range is applied as
+  // (factor * 2^15) then an exact 2^-15, so the factor itself never flushes
+  const bool tiny = fabsf(factor) < 6.103515625e-05f;
+  const __half2 f1 = __float2half2_rn(tiny ? factor * 32768.f : factor);
+  const __half2 f2 = __float2half2_rn(tiny ? 1.f / 32768.f : 1.f);
   __half2* w = reinterpret_cast<__half2*>(&v);
-  const float2 f2 = make_float2(factor, factor);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 z = __fmul2_rn(__half22float2(w[q]), f2);
-    w[q] = __floats2half2_rn(z.x, z.y);
-  }
+  for (int q = 0; q < 4; ++q) w[q] = __hmul2(__hmul2(w[q], f1), f2);
 }
 template <>
 __device__ __forceinline__ void vec_scale<float>(uint4& v, float factor) {
