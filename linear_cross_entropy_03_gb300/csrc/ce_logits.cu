@@ -804,6 +804,220 @@ cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, b
   return cudaLaunchKernelEx(&cfg, ce_rows_ring_kernel<T, VPT>, pc, depth);
 }
 
+// Half-row ring form, for rows of 72-144 KB (fp32 logits up to V = 36864,
+// 16-bit logits up to V = 73728): each row is loaded as two halves into a
+// ring of three half-row buffers; group g of the CTA takes half g of every
+// row (rows blockIdx.x, blockIdx.x + gridDim.x, ...), the CTA barrier joins
+// the two halves' partials, and each group writes its half's gradient.
+// Thread 0 keeps three half-rows in flight: after row j's barrier it
+// requests the second half of row j + 1 and the first half of row j + 2.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeParams p, uint32_t half_bytes) {
+  constexpr int EPV = 16 / sizeof(T);
+  extern __shared__ __align__(128) uint8_t ring_smem[];
+  __shared__ uint64_t full[3];
+  __shared__ float2 s_part[2][kRingWarps];  // per warp (max, sum of exp(z - max)), by row parity
+  __shared__ int s_last, s_abort;
+  __shared__ float s_gsum, s_gcomp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / kGroupWarps;
+  const int gtid = threadIdx.x % kGroupThreads;
+  const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
+  const uint32_t half_stride = (half_bytes + 127u) & ~127u;
+  const int nvec = static_cast<int>(row_bytes / 16);
+  const int hvec0 = static_cast<int>(half_bytes / 16);                 // vectors in the first half
+  const int hvec = grp == 0 ? hvec0 : nvec - hvec0;                     // vectors in this group's half
+  const int vbase = grp == 0 ? 0 : hvec0;                               // its first vector in the row
+  const int stride = gridDim.x;
+  const int n_rows = static_cast<int>(p.N);
+  const int mine = n_rows > static_cast<int>(blockIdx.x) ? (n_rows - 1 - static_cast<int>(blockIdx.x)) / stride + 1 : 0;
+  const uint32_t ring_base = smem_addr(ring_smem);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&full[i]), 1);
+    s_abort = 0;
+    s_gsum = s_gcomp = 0.f;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&s_abort, p.status, 2000000000ull};
+  // slot s = half s % 2 of the CTA's row s / 2, in buffer s % 3
+  int issued = 0;  // thread 0 only
+  auto issue_next = [&]() {
+    const int s = issued++;
+    const int j = s >> 1, h = s & 1;
+    if (j >= mine) return;
+    const int row = blockIdx.x + j * stride;
+    const uint32_t bytes = h == 0 ? half_bytes : row_bytes - half_bytes;
+    const uint32_t b = static_cast<uint32_t>(s % 3);
+    mbar_arrive_expect_tx(smem_addr(&full[b]), bytes);
+    bulk_load(ring_base + b * half_stride,
+              reinterpret_cast<const uint8_t*>(p.logits) + static_cast<int64_t>(row) * row_bytes + (h ? half_bytes : 0),
+              bytes, smem_addr(&full[b]));
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < 3; ++i) issue_next();
+  grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
+  const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
+
+  for (int j = 0; j < mine; ++j) {
+    const int row = blockIdx.x + j * stride;
+    const int64_t t = __ldg(p.target + row);
+    const float go = p.grad_out != nullptr ? __ldg(p.grad_out + row) : 1.f;
+    const int s = 2 * j + grp;
+    const int b = s % 3;
+    const bool ok = mbar_wait_sleep(smem_addr(&full[b]), static_cast<uint32_t>((s / 3) & 1), ctl);
+    uint4 v[VPT];
+    const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * half_stride);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int vi = i * kGroupThreads + gtid;
+      v[i] = vi < hvec ? sbuf[vi] : neg_inf_vec<T>();
+    }
+    const int64_t tcl = t - p.v_offset;
+    const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
+    const int tcol = valid ? static_cast<int>(tcl) : -1;
+    const int tvec = valid ? tcol / EPV - vbase : -1;  // the target's vector within this half
+    const bool own_t = valid && tvec >= 0 && tvec < hvec && (tvec % kGroupThreads) == gtid;
+    float zt = 0.f;
+    if (own_t) {
+      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i == t_i) zt = vec_get<T>(v[i], t_k);
+    }
+    const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
+    const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;
+    const float2 nmL = make_float2(nm, nm);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) vec_exp_acc<T>(v[i], nmL, acc);
+    const float sw = warp_sum(acc.x + acc.y);
+    if (lane == 0) s_part[j & 1][warp] = make_float2(mw, sw);
+    // one CTA barrier per row: it joins the halves' partials, frees both
+    // buffers and carries the abort vote
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {  // half-rows still in flight must land before leaving
+        for (int q = 2 * j; q < issued && q < 2 * mine; ++q)
+          mbar_wait_drain(smem_addr(&full[q % 3]), static_cast<uint32_t>((q / 3) & 1), 2000000000ull);
+      }
+      break;
+    }
+    if (threadIdx.x == 0) {
+      issue_next();
+      issue_next();
+    }
+    const float2 q = s_part[j & 1][lane];  // 32 warps: one partial per lane
+    const float M = warp_max(q.x);
+    const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
+    const float lse = M + logf(S);
+
+    if (p.lse_out != nullptr) {
+      if (own_t) p.zt_out[row] = zt;
+      if (threadIdx.x == 0) {
+        p.lse_out[row] = lse;
+        if (!valid) p.zt_out[row] = 0.f;
+      }
+      continue;
+    }
+    if (p.loss_out != nullptr) {  // the CTA's rows' losses, in row order (ordered by the CTA barriers)
+      if (own_t) {
+        const float y = (lse - zt) - s_gcomp;
+        const float t2 = s_gsum + y;
+        s_gcomp = (t2 - s_gsum) - y;
+        s_gsum = t2;
+      }
+    } else {
+      if (own_t) p.loss_rows[row] = lse - zt;
+      if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+    }
+    if (p.grad == nullptr) continue;
+    float scale = 0.f;
+    if (valid) {
+      if (p.reduction == FLCE_REDUCTION_MEAN)
+        scale = p.grad_scale / static_cast<float>(nv);
+      else if (p.reduction == FLCE_REDUCTION_SUM)
+        scale = p.grad_scale;
+      else
+        scale = p.grad_scale * go;
+    }
+    const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
+    if (own_t) {
+      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
+      const float dt = scale * (__expf(zt - lse) - 1.f);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i == t_i) vec_set<T>(v[i], t_k, dt);
+    }
+    uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + vbase + gtid;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
+  }
+
+  if (p.loss_out != nullptr) {  // as in the row-ring form: per-CTA partials, last CTA adds them
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      p.loss_rows[blockIdx.x] = s_gsum - s_gcomp;
+      __threadfence();
+      const unsigned int ticket = atomicAdd(p.ticket, 1u);
+      s_last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      float a = 0.f;
+      for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kRingThreads) a += __ldcg(p.loss_rows + i);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      __shared__ float s_acc[kRingWarps];
+      if (lane == 0) s_acc[warp] = a;
+      __syncthreads();
+      if (warp == 0) {
+        float total = s_acc[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        if (lane == 0) {
+          if (p.reduction == FLCE_REDUCTION_MEAN) {
+            const int n_valid = *p.n_valid;
+            p.loss_out[0] = n_valid > 0 ? total / static_cast<float>(n_valid) : __int_as_float(0x7fc00000);
+          } else {
+            p.loss_out[0] = total;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <typename T, int VPT>
+cudaError_t launch_half_t(const CeParams& p, uint32_t half_bytes, int grid, bool pdl, cudaStream_t s) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(ce_rows_half_kernel<T, VPT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kRingSmemBudget + 1024));
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kRingThreads);
+  cfg.dynamicSmemBytes = 3 * static_cast<size_t>((half_bytes + 127u) & ~127u);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  CeParams pc = p;
+  return cudaLaunchKernelEx(&cfg, ce_rows_half_kernel<T, VPT>, pc, half_bytes);
+}
+
 template <typename T, int EPV>
 cudaError_t launch_ce_t(const CeParams& p, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -875,6 +1089,25 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
           : vpt <= 8 ? launch_ring_t<float, 8>(p, depth, grid, smem, pdl, s)
                      : launch_ring_t<float, 10>(p, depth, grid, smem, pdl, s);
     }
+    prof_end(s);
+    return e;
+  }
+  // rows of 72-144 KB: the half-row ring form
+  const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
+  if (vector_path && row_bytes > 72 * 1024 && row_bytes <= 144 * 1024) {
+    const uint32_t half_bytes = static_cast<uint32_t>((row_bytes / 16 + 1) / 2 * 16);
+    const int vpt = static_cast<int>((half_bytes / 16 + kGroupThreads - 1) / kGroupThreads);
+    int grid = device_sm_count();
+    if (grid > p.N) grid = static_cast<int>(p.N);
+    if (dtype == FLCE_DTYPE_BF16)
+      e = vpt <= 8 ? launch_half_t<uint16_t, 8>(p, half_bytes, grid, pdl, s)
+                   : launch_half_t<uint16_t, 10>(p, half_bytes, grid, pdl, s);
+    else if (dtype == FLCE_DTYPE_FP16)
+      e = vpt <= 8 ? launch_half_t<__half, 8>(p, half_bytes, grid, pdl, s)
+                   : launch_half_t<__half, 10>(p, half_bytes, grid, pdl, s);
+    else
+      e = vpt <= 8 ? launch_half_t<float, 8>(p, half_bytes, grid, pdl, s)
+                   : launch_half_t<float, 10>(p, half_bytes, grid, pdl, s);
     prof_end(s);
     return e;
   }

@@ -55,7 +55,7 @@ def test_ce_config_1024x32768(dtype, reduction, in_place):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("n,v", [(37, 1000), (64, 8192), (5, 8191), (9, 100003), (3, 1), (20, 70000),
-                                 (16, 262144)])
+                                 (16, 262144), (33, 20004), (33, 40008)])
 def test_ce_shapes(dtype, n, v):
     logits, t = si.make_ce_logits(n, v, 100 + n, std=2.0, dtype=dtype, ignore_frac=0.2)
     ref = O.ce_reference(logits, t, reduction="mean")
