@@ -21,6 +21,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace cg = cooperative_groups;
@@ -361,15 +363,6 @@ __device__ __forceinline__ float vec_max<float>(const uint4& v) {
   return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
 }
 
-// Max over the vectors i of v with i * step < limit.
-template <typename T, int VPT>
-__device__ __forceinline__ float vec_max_all(const uint4 (&v)[VPT], int limit, int step) {
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < VPT; ++i)
-    if (i * step < limit) m = fmaxf(m, vec_max<T>(v[i]));
-  return m;
-}
 // bf16: the max of bf16 values is one of them, so it is taken exactly in one
 // running packed bf16x2 maximum, converted once at the end.
 template <int VPT>
@@ -384,22 +377,6 @@ __device__ __forceinline__ float vec_max_all_bf16(const uint4 (&v)[VPT], int lim
   }
   return fmaxf(__low2float(m), __high2float(m));
 }
-template <>
-__device__ __forceinline__ float vec_max_all<uint16_t, 2>(const uint4 (&v)[2], int limit, int step) {
-  return vec_max_all_bf16<2>(v, limit, step);
-}
-template <>
-__device__ __forceinline__ float vec_max_all<uint16_t, 4>(const uint4 (&v)[4], int limit, int step) {
-  return vec_max_all_bf16<4>(v, limit, step);
-}
-template <>
-__device__ __forceinline__ float vec_max_all<uint16_t, 8>(const uint4 (&v)[8], int limit, int step) {
-  return vec_max_all_bf16<8>(v, limit, step);
-}
-template <>
-__device__ __forceinline__ float vec_max_all<uint16_t, 10>(const uint4 (&v)[10], int limit, int step) {
-  return vec_max_all_bf16<10>(v, limit, step);
-}
 // fp16: the same running packed maximum in half2
 template <int VPT>
 __device__ __forceinline__ float vec_max_all_f16(const uint4 (&v)[VPT], int limit, int step) {
@@ -413,21 +390,21 @@ __device__ __forceinline__ float vec_max_all_f16(const uint4 (&v)[VPT], int limi
   }
   return fmaxf(__low2float(m), __high2float(m));
 }
-template <>
-__device__ __forceinline__ float vec_max_all<__half, 2>(const uint4 (&v)[2], int limit, int step) {
-  return vec_max_all_f16<2>(v, limit, step);
-}
-template <>
-__device__ __forceinline__ float vec_max_all<__half, 4>(const uint4 (&v)[4], int limit, int step) {
-  return vec_max_all_f16<4>(v, limit, step);
-}
-template <>
-__device__ __forceinline__ float vec_max_all<__half, 8>(const uint4 (&v)[8], int limit, int step) {
-  return vec_max_all_f16<8>(v, limit, step);
-}
-template <>
-__device__ __forceinline__ float vec_max_all<__half, 10>(const uint4 (&v)[10], int limit, int step) {
-  return vec_max_all_f16<10>(v, limit, step);
+
+// Max over the vectors i of v with i * step < limit.
+template <typename T, int VPT>
+__device__ __forceinline__ float vec_max_all(const uint4 (&v)[VPT], int limit, int step) {
+  if constexpr (std::is_same<T, uint16_t>::value) {
+    return vec_max_all_bf16<VPT>(v, limit, step);
+  } else if constexpr (std::is_same<T, __half>::value) {
+    return vec_max_all_f16<VPT>(v, limit, step);
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (i * step < limit) m = fmaxf(m, vec_max<T>(v[i]));
+    return m;
+  }
 }
 
 // Replaces every element z by exp(z - m) and adds the exponentials into the
