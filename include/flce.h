@@ -103,6 +103,12 @@ int64_t flce_default_chunk(int64_t N, int64_t H, int64_t V);
  * sizes. */
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction);
 
+/* flce_workspace_size_typed -- the workspace flce_fwd_bwd_typed needs for
+ * operands of `dtype` (flce_dtype_t); 0 for an unknown dtype or invalid
+ * sizes. */
+size_t flce_workspace_size_typed(int dtype, int64_t N, int64_t H, int64_t V, int64_t chunk,
+                                 int reduction);
+
 /*
  * flce_fwd_bwd -- loss and gradients of cross_entropy(hidden @ weight^T + bias, target).
  *
@@ -151,14 +157,17 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
 
 /*
  * flce_fwd_bwd_typed -- flce_fwd_bwd with the operand type given: dtype is
- * FLCE_DTYPE_BF16 (exactly flce_fwd_bwd) or FLCE_DTYPE_FP16, for which
- * hidden, weight, bias and grad_hidden are IEEE half (fp16) and everything
- * else is as in flce_fwd_bwd, same workspace size.  Other dtypes return
- * FLCE_ERR_UNSUPPORTED, and so does fp16 while the one-CTA GEMM form is
- * selected (flce_set_gemm_variant).  The logits dtypes FP32 / FP16 / BF16 the
- * DeepSpeed PR #8540 description ("optional Liger vocab-parallel CE
- * backend", section "Changes") validates carry over to the fused form for
- * the two 16-bit types.
+ *   FLCE_DTYPE_BF16  exactly flce_fwd_bwd;
+ *   FLCE_DTYPE_FP16  hidden, weight, bias and grad_hidden are IEEE half;
+ *   FLCE_DTYPE_FP32  hidden, weight, bias and grad_hidden are fp32;
+ * everything else is as in flce_fwd_bwd.  The workspace must hold
+ * flce_workspace_size_typed(dtype, ...) bytes (the same as
+ * flce_workspace_size for the two 16-bit types; fp32 adds room for the bf16
+ * copies of hidden, weight and bias).  Other dtypes return
+ * FLCE_ERR_UNSUPPORTED, and so does fp16 / fp32 while the one-CTA GEMM form
+ * is selected (flce_set_gemm_variant).  The logits dtypes FP32 / FP16 / BF16
+ * the DeepSpeed PR #8540 description ("optional Liger vocab-parallel CE
+ * backend", section "Changes") validates carry over to the fused form here.
  *
  * Arithmetic with fp16: fp16 x fp16 on the tensor cores with fp32
  * accumulation; the chunk logits are kept in fp16, and the chunk's
@@ -167,6 +176,14 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
  * NONE), so they lie in [-1, 1] rather than underflowing fp16's range; the
  * two backward products multiply that factor back in fp32.  grad_bias is
  * summed from the fp32 grad-logits.
+ *
+ * Arithmetic with fp32: hidden, weight and bias are rounded to bf16 (to
+ * nearest, ties to even) into the workspace once per call and the bf16 path
+ * runs on those copies, so the loss and grad_weight / grad_bias equal the
+ * bf16 entry point's on the rounded inputs; grad_hidden is written from the
+ * fp32 accumulator without the bf16 rounding.  (The mixed-precision recipe
+ * the fused kernel serves computes in 16-bit; fp32 operands are accepted for
+ * callers whose master copies are fp32.)
  */
 flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weight, const void* bias,
                                  const int64_t* target, int64_t N, int64_t H, int64_t V,

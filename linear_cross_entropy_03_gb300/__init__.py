@@ -17,7 +17,7 @@ from typing import Optional
 __all__ = [
     "REDUCTIONS", "DTYPES", "STATUS_BIT_TARGET_RANGE", "STATUS_BIT_TIMEOUT", "KERNEL_NAMES",
     "library_path", "lib", "flce_status_string", "flce_version", "flce_default_chunk",
-    "flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_typed", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
+    "flce_workspace_size", "flce_workspace_size_typed", "flce_fwd_bwd", "flce_fwd_bwd_typed", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
     "flce_vp_workspace_size", "flce_vp_forward", "flce_vp_backward", "ce_vp_partials", "ce_vp_backward",
     "flce_set_gemm_variant", "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
     "flce_profile_enable", "flce_profile_disable", "flce_profile_read",
@@ -43,6 +43,7 @@ _SIGNATURES = {
     "flce_version": (ctypes.c_int, []),
     "flce_default_chunk": (_I64, [_I64, _I64, _I64]),
     "flce_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, ctypes.c_int]),
+    "flce_workspace_size_typed": (_SZ, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int]),
     "flce_fwd_bwd": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_int, _I64,
                                     ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P,
                                     _P, _SZ, _P, _P]),
@@ -136,6 +137,10 @@ def flce_default_chunk(N: int, H: int, V: int) -> int:
 
 def flce_workspace_size(N: int, H: int, V: int, chunk: int = 0, reduction="mean") -> int:
     return lib().flce_workspace_size(N, H, V, chunk, _red(reduction))
+
+
+def flce_workspace_size_typed(dtype, N: int, H: int, V: int, chunk: int = 0, reduction="mean") -> int:
+    return lib().flce_workspace_size_typed(_dt(dtype), N, H, V, chunk, _red(reduction))
 
 
 def flce_fwd_bwd(hidden, weight, bias, target, N, H, V, ignore_index, reduction, chunk, grad_scale,
@@ -276,8 +281,8 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
                                row_stats: bool = False, workspace=None, status=None, stream=None) -> dict:
     """Loss and gradients of cross_entropy(hidden @ weight.T + bias, target).
 
-    hidden [N, H] and weight [V, H] bf16 or fp16 (both the same), bias [V] of
-    that type or None, target [N] int64, all on one CUDA device and
+    hidden [N, H] and weight [V, H] bf16, fp16 or fp32 (both the same), bias
+    [V] of that type or None, target [N] int64, all on one CUDA device and
     contiguous.  Returns a dict with ``loss`` (fp32 [N] or []),
     ``grad_hidden`` ([N, H], the input type), ``grad_weight``
     (fp32 [V, H]), ``grad_bias`` (fp32 [V]), ``n_valid`` (int32 [1]) and, with
@@ -291,9 +296,9 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
     dev = hidden.device
     red = _red(reduction)
     loss = torch.empty(n if red == 0 else 1, dtype=torch.float32, device=dev)
-    if hidden.dtype not in (torch.bfloat16, torch.float16) or weight.dtype != hidden.dtype:
-        raise FlceError(2, "fused_linear_cross_entropy: hidden and weight must both be bf16 or both fp16")
-    dtype = "fp16" if hidden.dtype == torch.float16 else "bf16"
+    dtype = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}.get(hidden.dtype)
+    if dtype is None or weight.dtype != hidden.dtype or (bias is not None and bias.dtype != hidden.dtype):
+        raise FlceError(2, "fused_linear_cross_entropy: hidden, weight and bias must share one of bf16/fp16/fp32")
     gh = torch.empty(n, h, dtype=hidden.dtype, device=dev) if grad_hidden else None
     gw = grad_weight_out if grad_weight_out is not None else (
         torch.empty(v, h, dtype=torch.float32, device=dev) if grad_weight else None)
@@ -302,9 +307,9 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
     nv = torch.zeros(1, dtype=torch.int32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev) if row_stats else None
     tl = torch.empty(n, dtype=torch.float32, device=dev) if row_stats else None
-    ws_bytes = flce_workspace_size(n, h, v, chunk, red)
+    ws_bytes = flce_workspace_size_typed(dtype, n, h, v, chunk, red)
     if ws_bytes == 0:
-        raise FlceError(1, "flce_workspace_size")
+        raise FlceError(1, "flce_workspace_size_typed")
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     if status is None:

@@ -78,6 +78,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int6
 struct FlceLayout {
   int64_t chunk, num_chunks, vp, nvt;
   size_t header, zbuf, partials, tgt_logit, row_lse, row_scale, row_tgt, loss_rows, total;
+  size_t cvt_h, cvt_w, cvt_b;  // fp32 operands: their bf16 copies (0 bytes otherwise)
 };
 
 int64_t default_chunk(int64_t N, int64_t V) {
@@ -89,7 +90,8 @@ int64_t default_chunk(int64_t N, int64_t V) {
   return c;
 }
 
-bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, FlceLayout* L) {
+bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, FlceLayout* L,
+                 int dtype = FLCE_DTYPE_BF16) {
   if (N < 0 || H < 8 || V < 1 || chunk < 0 || reduction < 0 || reduction > 2) return false;
   if (N >= (int64_t(1) << 31) || V >= (int64_t(1) << 31) || H >= (int64_t(1) << 24)) return false;
   L->chunk = chunk == 0 ? default_chunk(N, V) : chunk;
@@ -115,6 +117,13 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
   L->loss_rows = off;
   off = round_up(off + (reduction == FLCE_REDUCTION_NONE ? 0 : static_cast<size_t>(N) * 4), kAlign);
+  const bool f32 = dtype == FLCE_DTYPE_FP32;
+  L->cvt_h = off;
+  off = round_up(off + (f32 ? static_cast<size_t>(N) * H * 2 : 0), kAlign);
+  L->cvt_w = off;
+  off = round_up(off + (f32 ? static_cast<size_t>(V) * H * 2 : 0), kAlign);
+  L->cvt_b = off;
+  off = round_up(off + (f32 ? static_cast<size_t>(L->vp) * 2 : 0), kAlign);
   L->total = off;
   return true;
 }
@@ -188,6 +197,13 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk, int r
   return L.total;
 }
 
+size_t flce_workspace_size_typed(int dtype, int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction) {
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16 && dtype != FLCE_DTYPE_FP32) return 0;
+  FlceLayout L;
+  if (!flce_layout(N, H, V, chunk, reduction, &L, dtype)) return 0;
+  return L.total;
+}
+
 flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* bias, const int64_t* target,
                            int64_t N, int64_t H, int64_t V, int64_t ignore_index, int reduction,
                            int64_t chunk, float grad_scale, const float* grad_out_none, float* loss,
@@ -209,12 +225,13 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FlceLayout L;
   if (N < 0 || V < 1 || H < 1 || chunk < 0 || reduction < 0 || reduction > 2) return FLCE_ERR_INVALID_ARG;
-  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16) return FLCE_ERR_UNSUPPORTED;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16 && dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
   const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
   const bool fp16 = dtype == FLCE_DTYPE_FP16;
-  if (fp16 && !pair) return FLCE_ERR_UNSUPPORTED;  // fp16 operands: the CTA-pair kernels only
+  const bool fp32 = dtype == FLCE_DTYPE_FP32;
+  if ((fp16 || fp32) && !pair) return FLCE_ERR_UNSUPPORTED;  // fp16 / fp32 operands: the CTA-pair kernels only
   if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
-  if (!flce_layout(N, H, V, chunk, reduction, &L)) return FLCE_ERR_INVALID_ARG;
+  if (!flce_layout(N, H, V, chunk, reduction, &L, dtype)) return FLCE_ERR_INVALID_ARG;
   if (loss == nullptr || weight == nullptr) return FLCE_ERR_INVALID_ARG;
   if (N > 0 && (hidden == nullptr || target == nullptr)) return FLCE_ERR_INVALID_ARG;
   if (grad_bias != nullptr && bias == nullptr) return FLCE_ERR_INVALID_ARG;
@@ -249,6 +266,22 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     return FLCE_OK;
   }
 
+  if (fp32) {
+    // fp32 operands: the tensor cores take their bf16 roundings, copied once
+    // per call into the workspace (grad_hidden is still written in fp32)
+    uint16_t* h16 = reinterpret_cast<uint16_t*>(ws + L.cvt_h);
+    uint16_t* w16 = reinterpret_cast<uint16_t*>(ws + L.cvt_w);
+    FLCE_TRY_CUDA(launch_f32_to_bf16(static_cast<const float*>(hidden), h16, N * H, stream));
+    FLCE_TRY_CUDA(launch_f32_to_bf16(static_cast<const float*>(weight), w16, V * H, stream));
+    hidden = h16;
+    weight = w16;
+    if (bias != nullptr) {
+      uint16_t* b16 = reinterpret_cast<uint16_t*>(ws + L.cvt_b);
+      FLCE_TRY_CUDA(launch_f32_to_bf16(static_cast<const float*>(bias), b16, V, stream));
+      bias = b16;
+    }
+  }
+
   CUtensorMap tm_h, tm_w, tm_z;
   const CUtensorMapDataType mtype = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map(&tm_h, hidden, H, N, H, mtype) || !make_map(&tm_w, weight, H, V, H, mtype)) return FLCE_ERR_CUDA;
@@ -275,7 +308,8 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     g.partials = partials;
     g.nvt = static_cast<int>(L.nvt);
     g.tgt_logit = tgt_logit;
-    g.grad_hidden = static_cast<uint16_t*>(grad_hidden);
+    g.grad_hidden = fp32 ? nullptr : static_cast<uint16_t*>(grad_hidden);
+    g.grad_hidden_f32 = fp32 ? static_cast<float*>(grad_hidden) : nullptr;
     g.grad_weight = grad_weight;
     g.gw_store = (k == 0 && !accumulate) ? 1 : 0;
     g.status = status;

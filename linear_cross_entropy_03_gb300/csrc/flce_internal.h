@@ -166,6 +166,7 @@ cudaError_t launch_ce_vp_grad(const void* logits, void* grad, int dtype, const i
 cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,
                                float* loss, cudaStream_t s, bool pdl);
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool pdl, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 

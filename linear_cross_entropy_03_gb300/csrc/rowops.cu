@@ -339,6 +339,22 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// fp32 -> bf16 (round to nearest even), 8 elements per thread and step,
+// scalar tail; in and out 16-byte aligned.
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restrict__ in, uint16_t* __restrict__ out,
+                                                          int64_t n) {
+  const int64_t n8 = n / 8;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += step) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(in) + 2 * i);
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(in) + 2 * i + 1);
+    reinterpret_cast<uint4*>(out)[i] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
+  for (int64_t i = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += step)
+    out[i] = static_cast<uint16_t>(pack_bf16x2(in[i], 0.f) & 0xFFFFu);
+}
+
 constexpr int kReduceThreads = 1024;
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -505,6 +521,16 @@ cudaError_t launch_ce_vp_grad(const void* logits, void* grad, int dtype, const i
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n / 8 + 255) / 256;
+  const int64_t cap = 8LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  f32_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,

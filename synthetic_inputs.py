@@ -234,12 +234,14 @@ def make_flce_inputs(n: int, h: int, v: int, seed: int, *, h_std: float = 1.0,
                      ignore_frac: float = 0.05,
                      ignore_index: int = IGNORE_INDEX, dtype: str = "bf16") -> FlceInputs:
     """dtype "bf16": bf16 bit patterns; "fp16": float16 values (float64 draw ->
-    float32 -> float16, round to nearest even)."""
+    float32 -> float16, round to nearest even); "fp32": float32 values."""
     if dtype == "bf16":
         gen = normal_bf16
     elif dtype == "fp16":
         def gen(sd, st, shape, std):
             return normal_f32(sd, st, shape, std).astype(np.float16)
+    elif dtype == "fp32":
+        gen = normal_f32
     else:
         raise ValueError(dtype)
     hidden = gen(seed, _S_HIDDEN, (n, h), h_std)

@@ -22,8 +22,9 @@ def dev_bf16(bits: np.ndarray) -> torch.Tensor:
 
 
 def dev16(a: np.ndarray) -> torch.Tensor:
-    """bf16 bit patterns (uint16) or float16 values on the GPU, as bf16 / fp16."""
-    if a.dtype == np.float16:
+    """bf16 bit patterns (uint16), float16 or float32 values on the GPU, as
+    bf16 / fp16 / fp32."""
+    if a.dtype in (np.float16, np.float32):
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
     return dev_bf16(a)
 
@@ -82,14 +83,18 @@ def assert_grad(got, ref, name):
         assert err <= GRAD_RTOL * scale, f"{name}: max err {err:.3e} > {GRAD_RTOL} * {scale:.3e}"
 
 
-def assert_flce_parity(res, ref, reduction, *, check_grads=True):
+def assert_flce_parity(res, ref, reduction, *, check_grads=True, row_rtol=1e-5):
+    """row_rtol bounds the per-row lse / target logit error relative to the
+    largest |lse|: 1e-5 when the oracle sees the very operands the tensor
+    cores multiply (fp32 accumulation is all that differs), the loss
+    tolerance when the kernel rounds the operands first (fp32 inputs)."""
     assert res["status"] == 0, f"device status {res['status']:#x}"
     assert res["n_valid"] == ref["n_valid"]
     assert_loss(res["loss"], ref["loss"], reduction)
     valid = ref["valid"]
     lse_scale = max(1.0, np.abs(ref["lse"]).max())
-    assert np.abs(res["lse"] - ref["lse"]).max() <= 1e-5 * lse_scale
-    assert np.abs(res["target_logit"][valid] - ref["target_logit"][valid]).max(initial=0) <= 1e-5 * lse_scale
+    assert np.abs(res["lse"] - ref["lse"]).max() <= row_rtol * lse_scale
+    assert np.abs(res["target_logit"][valid] - ref["target_logit"][valid]).max(initial=0) <= row_rtol * lse_scale
     assert np.all(res["target_logit"][~valid] == 0.0)
     if reduction == "none":
         assert np.all(res["loss"][~valid] == 0.0), "ignored rows must carry exactly zero loss"

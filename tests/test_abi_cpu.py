@@ -71,10 +71,23 @@ def test_flce_typed_rejects_other_dtypes(lib):
                 reduction=2, chunk=0, grad_scale=1.0, grad_out_none=None, loss=FAKE, grad_hidden=None,
                 grad_weight=None, grad_bias=None, accumulate=0, n_valid_out=None, lse_out=None,
                 target_logit_out=None, workspace=FAKE, workspace_bytes=1 << 40, status_dev=None, stream=0)
-    assert flce.flce_fwd_bwd_typed("fp32", **base) == 2
     assert flce.flce_fwd_bwd_typed(7, **base) == 2
-    assert flce.flce_fwd_bwd_typed("fp16", **dict(base, N=-1)) == 1
-    assert flce.flce_fwd_bwd_typed("fp16", **dict(base, hidden=FAKE + 8)) == 7
+    assert flce.flce_fwd_bwd_typed(-1, **base) == 2
+    for dt in ("fp16", "fp32"):
+        assert flce.flce_fwd_bwd_typed(dt, **dict(base, N=-1)) == 1
+        assert flce.flce_fwd_bwd_typed(dt, **dict(base, hidden=FAKE + 8)) == 7
+        assert flce.flce_fwd_bwd_typed(dt, **dict(base, workspace_bytes=100)) == 3
+
+
+def test_flce_typed_workspace_holds_fp32_copies(lib):
+    n, h, v = 1000, 256, 5000
+    base = flce.flce_workspace_size(n, h, v, 0, "mean")
+    assert flce.flce_workspace_size_typed("bf16", n, h, v, 0, "mean") == base
+    assert flce.flce_workspace_size_typed("fp16", n, h, v, 0, "mean") == base
+    f32 = flce.flce_workspace_size_typed("fp32", n, h, v, 0, "mean")
+    assert base + 2 * (n * h + v * h + v) <= f32 <= base + 2 * (n * h + v * h + v) + 3 * 256 + 2 * 64
+    assert flce.flce_workspace_size_typed(7, n, h, v, 0, "mean") == 0
+    assert flce.flce_workspace_size_typed("fp32", -1, h, v, 0, "mean") == 0
 
 
 def _ce(**kw):
