@@ -268,48 +268,71 @@ def kernel_profile(flce, records):
     return agg
 
 
-def ce_bandwidth(step, iters=20):
-    """ce_fwd_bwd alone, L2 emptied before every call: a 256 MB buffer is
-    written, then another 256 MB read, so the call finds none of its data in
-    L2 and no dirty lines of the flush to write back.  A short device sleep
-    keeps the GPU busy while the host enqueues the call, so the call's time
-    excludes the host's launch cost.  Returns the median time of the whole
-    call (library profiling off) and of its ce_rows kernel (library events,
-    a separate loop)."""
+class L2Emptier:
+    """Empties L2 before a timed call: a 256 MB buffer is written, then
+    another 256 MB read, so the call finds none of its data in L2 and no dirty
+    lines of the flush to write back.  A short device sleep then keeps the GPU
+    busy while the host enqueues the call, so the call's time excludes the
+    host's launch cost."""
+
+    def __init__(self, device):
+        import torch
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        self.clean = torch.zeros(64 << 20, dtype=torch.float32, device=device)
+        self.sleep = getattr(torch.cuda, "_sleep", None)
+
+    def __call__(self, i):
+        self.flush.fill_(i & 0xFF)
+        self.clean.sum()
+        if self.sleep is not None:
+            self.sleep(200000)
+
+
+def time_call(flce, call, empty_l2, iters=20, kernels=("ce_rows",)):
+    """Median time of `call` with L2 emptied before each (library profiling
+    off), and median of the summed durations of its `kernels` (library
+    events, a separate loop; None when kernels is empty)."""
     import torch
-    flce = step.flce
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=step.ws.device)
-    clean = torch.zeros(64 << 20, dtype=torch.float32, device=step.ws.device)
-    sleep = getattr(torch.cuda, "_sleep", None)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-    def empty_l2(i):
-        flush.fill_(i & 0xFF)
-        clean.sum()
-        if sleep is not None:
-            sleep(200000)
-
     times, kernel = [], []
     for i in range(iters + 3):
         empty_l2(i)
         a.record()
-        step.ce_call()
+        call()
         b.record()
         torch.cuda.synchronize()
         if i >= 3:
             times.append(a.elapsed_time(b))
+    if not kernels:
+        return statistics.median(times), None
     for i in range(iters + 3):
         flce.flce_profile_enable(16)
         empty_l2(i)
-        step.ce_call()
+        call()
         torch.cuda.synchronize()
         rec = flce.flce_profile_read(16)
         flce.flce_profile_disable()
         if i >= 3:
-            kernel.append(sum(ms for name, ms in rec if name == "ce_rows"))
+            kernel.append(sum(ms for name, ms in rec if name in kernels))
+    return statistics.median(times), statistics.median(kernel)
+
+
+def ce_bandwidth(step, iters=20):
+    """ce_fwd_bwd alone on the CE workload, L2 emptied before every call.
+    Returns the median time of the whole call and of its ce_rows kernel, the
+    algorithmic bytes, and the median time of a plain device-to-device copy
+    of the same bytes (torch's copy, one read and one write of every logit,
+    timed the same way): the attainable time for that much traffic at this
+    size, launch and ramp included."""
+    import torch
+    empty_l2 = L2Emptier(step.ws.device)
+    call_ms, kernel_ms = time_call(step.flce, step.ce_call, empty_l2, iters)
     cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
+    src = torch.empty(cn * cv, dtype=torch.bfloat16, device=step.ws.device).fill_(1.0)
+    dst = torch.empty_like(src)
+    copy_ms, _ = time_call(step.flce, lambda: dst.copy_(src), empty_l2, iters, kernels=())
     alg_bytes = 2 * cn * cv * 2 + 12 * cn
-    return statistics.median(times), statistics.median(kernel), alg_bytes
+    return call_ms, kernel_ms, alg_bytes, copy_ms
 
 
 def e2e_steps(step, host, dev, steps, warmup, barrier):
@@ -400,7 +423,7 @@ def _device_ms(fn, steps, warmup):
 
 def next_rows(step, steps=5, warmup=3):
     """The widened rows on the same shapes, fewer steps: forward-only FLCE,
-    FLCE with fp16 operands, FLCE on one vocabulary shard of two (forward
+    FLCE with fp16 operands, with fp32 operands, FLCE on one vocabulary shard of two (forward
     partials + backward from given row statistics, every chunk), CE on fp16 /
     fp32 logits, CE on two vocabulary shards (partials + backward)."""
     import torch
@@ -440,6 +463,22 @@ def next_rows(step, steps=5, warmup=3):
                         "frac_of_bf16_peak": round(tf / peak_tf, 4)}
     del h16, w16, gh16
 
+    # fp32 hidden / weight (rounded to bf16 copies inside the call), fp32 grad_hidden
+    h32, w32 = d["hidden"].float(), d["weight"].float()
+    gh32f = torch.empty(n, h, dtype=torch.float32, device=dev)
+    ws32_bytes = flce.flce_workspace_size_typed("fp32", n, h, v, chunk, step.red)
+    ws32 = torch.empty(ws32_bytes, dtype=torch.uint8, device=dev)
+
+    def fp32_step():
+        check(flce.flce_fwd_bwd_typed("fp32", h32, w32, None, d["target"], n, h, v, -100, step.red, chunk, 1.0,
+                                      None, step.loss, gh32f, step.grad_weight, None, 0, None, None, None, ws32,
+                                      ws32_bytes, step.status, step.stream), "fp32")
+    ms = _device_ms(fp32_step, steps, warmup)
+    tf = 6.0 * n * h * v / (ms / 1e3) / 1e12
+    out["flce_fp32_operands"] = {"tokens_per_s": round(n / (ms / 1e3), 1), "ms": round(ms, 3),
+                                 "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak_tf, 4)}
+    del h32, w32, gh32f, ws32
+
     # one vocabulary shard of two: per chunk, the shard's forward partials, then
     # its backward from row statistics (here the shard's own; the combine is the caller's)
     vs = v // 2
@@ -468,32 +507,20 @@ def next_rows(step, steps=5, warmup=3):
 
     # CE on fp16 / fp32 logits and on two vocabulary shards (L2 emptied before each call)
     cn, cv = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    clean = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    empty_l2 = L2Emptier(dev)
     tgt = d["ce_target"]
     ws = torch.empty(flce.ce_workspace_size(cn, cv, "fp32", "mean"), dtype=torch.uint8, device=dev)
     loss = torch.empty(1, device=dev)
 
-    def ce_ms(call, iters=20):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        times = []
-        for i in range(iters + 3):
-            flush.fill_(i & 0xFF)
-            clean.sum()
-            a.record()
-            call()
-            b.record()
-            torch.cuda.synchronize()
-            if i >= 3:
-                times.append(a.elapsed_time(b))
-        return statistics.median(times)
-
     for name, tdt, b in (("fp16", torch.float16, 2), ("fp32", torch.float32, 4)):
         z = d["logits"].to(tdt)
-        ms = ce_ms(lambda: check(flce.ce_fwd_bwd(z, name, z, tgt, cn, cv, -100, "mean", 1.0, None, loss, ws,
-                                                 ws.numel(), step.status, step.stream), "ce " + name))
-        gbs = (2 * cn * cv * b + 12 * cn) / (ms / 1e3) / 1e9
-        out[f"ce_logits_{name}"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+        ms, kms = time_call(flce, lambda: check(flce.ce_fwd_bwd(z, name, z, tgt, cn, cv, -100, "mean", 1.0, None,
+                                                                 loss, ws, ws.numel(), step.status, step.stream),
+                                                "ce " + name), empty_l2)
+        nbytes = 2 * cn * cv * b + 12 * cn
+        out[f"ce_logits_{name}"] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                                    "frac": round(nbytes / (ms / 1e3) / 1e9 / hbm, 4), "kernel_ms": round(kms, 4),
+                                    "kernel_frac": round(nbytes / (kms / 1e3) / 1e9 / hbm, 4)}
         del z
     half = cv // 2
     shards = [d["logits"][:, :half].contiguous(), d["logits"][:, half:].contiguous()]
@@ -510,7 +537,7 @@ def next_rows(step, steps=5, warmup=3):
         for k, zs in enumerate(shards):
             check(flce.ce_vp_backward(zs, "bf16", zs, tgt, cn, half, k * half, -100, comb, rs, step.status,
                                       step.stream), "ce vp backward")
-    ms = ce_ms(ce_vp)
+    ms, _ = time_call(flce, ce_vp, empty_l2, kernels=())
     gbs = (2 * cn * cv * 2 + 12 * cn) / (ms / 1e3) / 1e9
     out["ce_vp_two_shards"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
                                "note": "two passes over each shard (partials, then gradient) plus the combine"}
@@ -700,12 +727,12 @@ def main():
     # cap imposed during the GEMM loop has lifted; its own clocks are recorded
     ce_clocks = None
     if args.only_flce:
-        ce_ms, ce_kernel_ms, ce_bytes = float("nan"), float("nan"), 0
+        ce_ms, ce_kernel_ms, ce_bytes, copy_ms = float("nan"), float("nan"), 0, float("nan")
     else:
         time.sleep(0.5)
         sampler = ClockSampler(local)
         sampler.start()
-        ce_ms, ce_kernel_ms, ce_bytes = ce_bandwidth(step, iters=100)
+        ce_ms, ce_kernel_ms, ce_bytes, copy_ms = ce_bandwidth(step, iters=100)
         ce_clocks = sampler.stop()
     ce_gbs = ce_bytes / (ce_ms / 1e3) / 1e9
     ce_kernel_gbs = ce_bytes / (ce_kernel_ms / 1e3) / 1e9 if ce_kernel_ms > 0 else float("nan")
@@ -745,6 +772,13 @@ def main():
                              "kernel": "ce_rows", "kernel_ms": round(ce_kernel_ms, 4),
                              "kernel_gbs": round(ce_kernel_gbs, 1),
                              "kernel_frac": round(ce_kernel_gbs / peaks.get("hbm_gbs", 6800.0), 4),
+                             "copy_same_bytes": {"ms": round(copy_ms, 4),
+                                                 "gbs": round(ce_bytes / (copy_ms / 1e3) / 1e9, 1),
+                                                 "frac": round(ce_bytes / (copy_ms / 1e3) / 1e9 /
+                                                               peaks.get("hbm_gbs", 6800.0), 4),
+                                                 "kernel_frac_of_copy": round(copy_ms / ce_kernel_ms, 4),
+                                                 "what": "torch device-to-device copy of the 64 MB logits "
+                                                         "into another buffer, timed the same way"},
                              "l2": "emptied before every call (256 MB written, then 256 MB read)", "scope": "gbs/frac: whole ce_fwd_bwd call "
                              "(count + ce_rows kernels); kernel_*: ce_rows alone", "clocks": ce_clocks},
             "scratch": {"workspace_bytes": step.ws_bytes, "peak_allocated_delta_bytes": peak_delta,

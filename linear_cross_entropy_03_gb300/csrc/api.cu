@@ -4,6 +4,7 @@
 // caller's stream.
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <mutex>
 #include <vector>
 
@@ -129,7 +130,7 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
 }
 
 struct CeLayout {
-  size_t header, loss_rows, total;
+  size_t header, loss_rows, flags, total;
 };
 
 bool ce_layout(int64_t N, int64_t V, int dtype, int reduction, CeLayout* L) {
@@ -138,8 +139,19 @@ bool ce_layout(int64_t N, int64_t V, int dtype, int reduction, CeLayout* L) {
     return false;
   L->header = 0;
   L->loss_rows = round_up(sizeof(WorkspaceHeader) + 16, kAlign);
-  L->total = round_up(L->loss_rows + static_cast<size_t>(N) * 4, kAlign);
+  L->flags = round_up(L->loss_rows + static_cast<size_t>(N) * 4, kAlign);
+  L->total = round_up(L->flags + sizeof(unsigned long long), kAlign);
   return true;
+}
+
+// A 40-bit value no recent call of this process used: the single-launch CE
+// form tags its arrival counter with it (the word it finds in the workspace
+// is some earlier call's, or whatever the memory held).
+unsigned long long next_ce_nonce() {
+  static std::atomic<unsigned long long> counter{
+      0x9E3779B97F4A7C15ull ^
+      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
+  return (counter.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
 }
 
 #define FLCE_TRY_CUDA(expr)                  \
@@ -412,6 +424,32 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
   int* status = status_dev != nullptr ? status_dev : &hdr->status;
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
 
+  const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned(logits, 16) &&
+                   (grad_logits == nullptr || aligned(grad_logits, 16));
+  if (N > 0 && N <= kCeSelfCountMaxRows && ce_rows_single_launch_ok(V, dtype, vec)) {
+    // one launch: the row kernel counts the targets itself and finds the CTA
+    // that adds the loss partials by flags, so nothing needs zeroing first
+    CeParams p = {};
+    p.logits = logits;
+    p.grad = grad_logits;
+    p.target = target;
+    p.N = N;
+    p.V = V;
+    p.ignore_index = ignore_index;
+    p.reduction = reduction;
+    p.grad_scale = grad_scale;
+    p.grad_out = grad_out_none;
+    p.loss_rows = loss_rows;
+    p.status = status_dev;
+    p.cluster = 1;
+    p.seg_len = V;
+    p.loss_out = reduction != FLCE_REDUCTION_NONE ? loss : nullptr;
+    p.self_count = 1;
+    p.done_flags = reinterpret_cast<unsigned long long*>(ws + L.flags);
+    p.nonce = next_ce_nonce();
+    FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, false, stream));
+    return FLCE_OK;
+  }
   if (N <= kCountSingleBlockMax) {
     // one block zeroes the header and counts; the CE kernel overlaps it (PDL)
     FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 1, status, nullptr, nullptr, 0, nullptr, stream));
@@ -420,8 +458,6 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
     FLCE_TRY_CUDA(launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, nullptr, stream));
   }
   if (N > 0) {
-    const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned(logits, 16) &&
-                     (grad_logits == nullptr || aligned(grad_logits, 16));
     const int64_t cap = ce_cta_capacity(dtype, vec);
     const int64_t epv = ce_vector_elems(dtype, vec);
     int64_t cl = ceil_div(V, cap);

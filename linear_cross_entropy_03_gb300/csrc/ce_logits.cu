@@ -528,6 +528,90 @@ __device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool 
   return r != 0;
 }
 
+// Single-launch form: the number of valid targets over all N rows, counted
+// by the whole CTA (every CTA does the same), and the out-of-range flag
+// (raised by CTA 0).  t_first is target[threadIdx.x] (or anything past N),
+// loaded by the caller before it requested the first rows, so that load is
+// ahead of them in the memory queue.  All threads of the CTA must call it.
+__device__ int cta_count_valid(const CeParams& p, int64_t t_first) {
+  int total = 0;
+  bool bad = false;
+  for (int64_t base = 0; base < p.N; base += blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    bool valid = false;
+    if (i < p.N) {
+      const int64_t t = base == 0 ? t_first : __ldg(p.target + i);
+      if (t != p.ignore_index) {
+        valid = t >= 0 && t < p.V;
+        bad |= !valid;
+      }
+    }
+    total += __syncthreads_count(valid);
+  }
+  if (__syncthreads_or(bad) && blockIdx.x == 0 && threadIdx.x == 0 && p.status != nullptr)
+    atomicOr(p.status, FLCE_STATUS_BIT_TARGET_RANGE);
+  return total;
+}
+
+// Single-launch form: the arrival counter that finds the last CTA needs no
+// zeroing beforehand.  Its 64-bit word holds (call nonce, CTAs arrived); CTA
+// 0 sets it to (nonce, 0) when it starts, and every CTA adds 1 when it ends.
+// An add that returns another tag came before that reset (which wiped it
+// out): the CTA waits for the reset to show, then adds again.  Returns the
+// number of CTAs arrived so far including this one (0 if the reset never
+// showed within the time limit; the status word then has the timeout bit).
+constexpr int kArrivalCountBits = 24;
+__device__ __forceinline__ unsigned long long arrival_tag(unsigned long long nonce) {
+  return nonce << kArrivalCountBits;
+}
+__device__ unsigned int arrive_tagged(unsigned long long* word, unsigned long long nonce, int* status) {
+  const unsigned long long tag = arrival_tag(nonce);
+  const unsigned long long mask = (1ull << kArrivalCountBits) - 1;
+  for (int attempt = 0; attempt < 4; ++attempt) {
+    const unsigned long long old = atomicAdd(word, 1ull);
+    if ((old & ~mask) == tag) return static_cast<unsigned int>((old & mask) + 1);
+    const uint64_t t0 = global_timer_ns();
+    while ((ld_relaxed_u64(word) & ~mask) != tag) {
+      if (global_timer_ns() - t0 > 2000000000ull) {
+        if (status != nullptr) atomicOr(status, FLCE_STATUS_BIT_TIMEOUT);
+        return 0;
+      }
+      __nanosleep(256);
+    }
+  }
+  return 0;  // not reached: the reset happens once per call
+}
+
+// Sum / mean: the CTA's loss partial goes to loss_rows[blockIdx.x] and the
+// last CTA to arrive adds all partials (lane order, then a fixed shuffle
+// tree, so the sum does not depend on which CTA it is) and writes loss_out.
+// Arrivals are counted on the zeroed ticket, or in the single-launch form
+// on the tagged counter.  Called by every thread after the CTA's
+// partial is final; warp 0 does the work.
+__device__ void ce_finish_loss(const CeParams& p, float part, int nv) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int grid = static_cast<int>(gridDim.x);
+  unsigned int arrived = 0;
+  if (lane == 0) {
+    p.loss_rows[blockIdx.x] = part;
+    __threadfence();
+    arrived = p.done_flags == nullptr ? atomicAdd(p.ticket, 1u) + 1u : arrive_tagged(p.done_flags, p.nonce, p.status);
+  }
+  if (__shfl_sync(0xffffffffu, arrived, 0) != static_cast<unsigned int>(grid)) return;
+  __threadfence();
+  float a = 0.f;
+  for (int i = lane; i < grid; i += 32) a += ld_relaxed_f32(p.loss_rows + i);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+  if (lane == 0) {
+    if (p.reduction == FLCE_REDUCTION_MEAN)
+      p.loss_out[0] = nv > 0 ? a / static_cast<float>(nv) : __int_as_float(0x7fc00000);
+    else
+      p.loss_out[0] = a;
+  }
+}
+
 // Two independent groups of kGroupThreads threads share the CTA's ring and
 // take alternate rows, each synchronising on its own named barrier, so one
 // group's reductions and stores overlap the other's waits.
@@ -542,7 +626,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   __shared__ uint64_t full[kRingMaxDepth];
   __shared__ int s_issued[kRingMaxDepth];  // loads issued into each buffer so far
   __shared__ float2 s_part[kRingGroups][2][kGroupWarps];  // per warp (max, sum of exp(z - max))
-  __shared__ int s_last, s_abort;
+  __shared__ int s_abort;
   __shared__ float s_gsum[kRingGroups], s_gcomp[kRingGroups];  // per group: compensated sum of its row losses
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / kGroupWarps, gwarp = warp % kGroupWarps;
@@ -589,11 +673,19 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       if (c > 0) mbar_wait_drain(smem_addr(&full[bi]), static_cast<uint32_t>((c - 1) & 1), 2000000000ull);
     }
   };
-  if (threadIdx.x == 0)
+  const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
+  if (threadIdx.x == 0) {
     for (int i = 0; i < first && i < mine; ++i) issue(i, blockIdx.x + i * stride);
+    if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+  }
   const bool full_rows = nvec == VPT * kGroupThreads;  // no vector past the row's end
-  grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
-  const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
+  int nv = 1;
+  if (p.self_count) {
+    nv = cta_count_valid(p, t_first);  // while the first rows load
+  } else {
+    grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
+    if (p.reduction == FLCE_REDUCTION_MEAN) nv = *p.n_valid;
+  }
 
   // this group's rows: j = grp, grp + 2, ...; a row's scalars are loaded
   // before its data is waited for
@@ -715,43 +807,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   // the other group gave up: copies it would have consumed must land first
   if (gtid == 0 && *static_cast<volatile int*>(&s_abort)) drain();
 
-  // sum / mean: each CTA leaves its partial in loss_rows[blockIdx.x] (the
-  // per-row losses are not needed); the last CTA adds the partials in a fixed
-  // tree order, so the result does not depend on which CTA finishes last
+  // sum / mean: the CTA's partial (the per-row losses are not needed), then
+  // one CTA adds the partials
   if (p.loss_out != nullptr) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-      float part = 0.f;
-      for (int q = 0; q < kRingGroups; ++q) part += s_gsum[q] - s_gcomp[q];
-      p.loss_rows[blockIdx.x] = part;
-      __threadfence();
-      const unsigned int ticket = atomicAdd(p.ticket, 1u);
-      s_last = ticket == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      float acc = 0.f;
-      for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kRingThreads) acc += __ldcg(p.loss_rows + i);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      __shared__ float s_acc[kRingWarps];
-      if (lane == 0) s_acc[warp] = acc;
-      __syncthreads();
-      if (warp == 0) {
-        float total = s_acc[lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-        if (lane == 0) {
-          if (p.reduction == FLCE_REDUCTION_MEAN) {
-            const int n_valid = *p.n_valid;
-            p.loss_out[0] = n_valid > 0 ? total / static_cast<float>(n_valid) : __int_as_float(0x7fc00000);
-          } else {
-            p.loss_out[0] = total;
-          }
-        }
-      }
-    }
+    float part = 0.f;
+    for (int q = 0; q < kRingGroups; ++q) part += s_gsum[q] - s_gcomp[q];
+    ce_finish_loss(p, part, nv);
   }
 }
 
@@ -794,7 +856,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
   extern __shared__ __align__(128) uint8_t ring_smem[];
   __shared__ uint64_t full[3];
   __shared__ float2 s_part[2][kRingWarps];  // per warp (max, sum of exp(z - max)), by row parity
-  __shared__ int s_last, s_abort;
+  __shared__ int s_abort;
   __shared__ float s_gsum, s_gcomp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = warp / kGroupWarps;
@@ -832,10 +894,18 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
               reinterpret_cast<const uint8_t*>(p.logits) + static_cast<int64_t>(row) * row_bytes + (h ? half_bytes : 0),
               bytes, smem_addr(&full[b]));
   };
-  if (threadIdx.x == 0)
+  const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
+  if (threadIdx.x == 0) {
     for (int i = 0; i < 3; ++i) issue_next();
-  grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
-  const int nv = p.reduction == FLCE_REDUCTION_MEAN ? *p.n_valid : 1;
+    if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+  }
+  int nv = 1;
+  if (p.self_count) {
+    nv = cta_count_valid(p, t_first);  // while the first half-rows load
+  } else {
+    grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
+    if (p.reduction == FLCE_REDUCTION_MEAN) nv = *p.n_valid;
+  }
 
   for (int j = 0; j < mine; ++j) {
     const int row = blockIdx.x + j * stride;
@@ -934,38 +1004,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
       if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
   }
 
-  if (p.loss_out != nullptr) {  // as in the row-ring form: per-CTA partials, last CTA adds them
+  if (p.loss_out != nullptr) {  // as in the row-ring form: the CTA's partial, then one CTA adds them
     __syncthreads();
-    if (threadIdx.x == 0) {
-      p.loss_rows[blockIdx.x] = s_gsum - s_gcomp;
-      __threadfence();
-      const unsigned int ticket = atomicAdd(p.ticket, 1u);
-      s_last = ticket == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      float a = 0.f;
-      for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kRingThreads) a += __ldcg(p.loss_rows + i);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      __shared__ float s_acc[kRingWarps];
-      if (lane == 0) s_acc[warp] = a;
-      __syncthreads();
-      if (warp == 0) {
-        float total = s_acc[lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-        if (lane == 0) {
-          if (p.reduction == FLCE_REDUCTION_MEAN) {
-            const int n_valid = *p.n_valid;
-            p.loss_out[0] = n_valid > 0 ? total / static_cast<float>(n_valid) : __int_as_float(0x7fc00000);
-          } else {
-            p.loss_out[0] = total;
-          }
-        }
-      }
-    }
+    ce_finish_loss(p, s_gsum - s_gcomp, nv);
   }
 }
 
@@ -1025,6 +1066,11 @@ int64_t ce_cta_capacity(int dtype, bool vector_path) {
 
 int64_t ce_vector_elems(int dtype, bool vector_path) {
   return vector_path ? (dtype == FLCE_DTYPE_FP32 ? 4 : 8) : 1;
+}
+
+bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path) {
+  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
+  return vector_path && row_bytes <= 144 * 1024 && device_sm_count() <= kCeMaxFlags;
 }
 
 // Row-ring form when rows fit (see above); 0 when it does not apply.

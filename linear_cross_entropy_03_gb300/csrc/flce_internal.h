@@ -114,7 +114,19 @@ struct CeParams {
   float* lse_out;           // partials mode (vocabulary shard): per-row LSE here, no gradient
   float* zt_out;            // partials mode: target logit if the target is in this shard, else 0
   int64_t v_offset;         // global id of this shard's first column
+  // single-launch form (no count kernel, nothing zeroed beforehand): every CTA
+  // counts the valid targets itself, and the last CTA to finish is found by
+  // an arrival counter that CTA 0 tags with this call's nonce, instead of a
+  // zeroed ticket
+  int self_count;
+  unsigned long long* done_flags;  // the tagged counter (one word), or null: use `ticket`
+  unsigned long long nonce;        // below 2^40, different from the previous call's
 };
+
+// Most rows the single-launch CE form takes (each CTA reads every target).
+constexpr int64_t kCeSelfCountMaxRows = 16384;
+// Most CTAs the single-launch form's arrival counter can count.
+constexpr int kCeMaxFlags = 1 << 20;
 
 // fp16 operands: the part of every row's gradient scale that is the same for
 // all rows (mean: g / n_valid; sum: g; none: g * max |grad_out|, or g).  The
@@ -168,6 +180,9 @@ cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction,
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool pdl, cudaStream_t s);
+// Whether rows of V elements go to a form that supports the single launch
+// (the row-ring or half-row kernel), and at most how many CTAs it launches.
+bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 
 int gemm_max_smem_ok();  // sets kernel attributes once per device; 0 on failure

@@ -55,7 +55,7 @@ def test_ce_config_1024x32768(dtype, reduction, in_place):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("n,v", [(37, 1000), (64, 8192), (5, 8191), (9, 100003), (3, 1), (20, 70000),
-                                 (16, 262144), (33, 20004), (33, 40008)])
+                                 (16, 262144), (33, 20004), (33, 40008), (20000, 64)])
 def test_ce_shapes(dtype, n, v):
     logits, t = si.make_ce_logits(n, v, 100 + n, std=2.0, dtype=dtype, ignore_frac=0.2)
     ref = O.ce_reference(logits, t, reduction="mean")
@@ -91,3 +91,35 @@ def test_ce_empty():
     out = flce.cross_entropy(z, torch.empty(0, dtype=torch.int64, device="cuda"), reduction="sum")
     torch.cuda.synchronize()
     assert out["loss"].item() == 0.0
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_ce_workspace_reused_and_dirty(reduction):
+    # the single-launch form finds the CTA that adds the loss partials by
+    # per-CTA flags set to the call's nonce: a workspace full of garbage, and
+    # one left by an earlier call on other data, must not be mistaken for done
+    n, v = 1024, 32768
+    ws = torch.full((flce.ce_workspace_size(n, v, "bf16", reduction),), 0xFF, dtype=torch.uint8, device="cuda")
+    for seed in (11, 12, 13):
+        logits, t = si.make_ce_logits(n, v, seed, std=2.0, dtype="bf16", ignore_frac=0.05)
+        ref = O.ce_reference(logits, t, reduction=reduction)
+        out = flce.cross_entropy(dev_bf16(logits), torch.from_numpy(t).cuda(), reduction=reduction,
+                                 workspace=ws)
+        torch.cuda.synchronize()
+        assert int(out["status"].item()) == 0
+        assert_loss(host(out["loss"]), ref["loss"], reduction)
+        assert_grad(host(out["grad_logits"]), ref["dz"], "grad_logits")
+
+
+def test_ce_without_status_word():
+    logits, t = si.make_ce_logits(300, 4000, 21, dtype="fp32")
+    ref = O.ce_reference(logits, t, reduction="mean")
+    z = torch.from_numpy(logits).cuda()
+    loss = torch.empty(1, device="cuda")
+    ws = torch.empty(flce.ce_workspace_size(300, 4000, "fp32", "mean"), dtype=torch.uint8, device="cuda")
+    st = flce.ce_fwd_bwd(z, "fp32", z, torch.from_numpy(t).cuda(), 300, 4000, -100, "mean", 1.0, None, loss,
+                         ws, ws.numel(), None, None)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert_loss(host(loss)[0], ref["loss"], "mean")
+    assert_grad(host(z), ref["dz"], "grad_logits")
