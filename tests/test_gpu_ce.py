@@ -55,7 +55,8 @@ def test_ce_config_1024x32768(dtype, reduction, in_place):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("n,v", [(37, 1000), (64, 8192), (5, 8191), (9, 100003), (3, 1), (20, 70000),
-                                 (16, 262144), (33, 20004), (33, 40008), (20000, 64)])
+                                 (16, 262144), (33, 20004), (33, 40008), (20000, 64), (1, 32768),
+                                 (2000, 8), (16384, 72), (16385, 72)])
 def test_ce_shapes(dtype, n, v):
     logits, t = si.make_ce_logits(n, v, 100 + n, std=2.0, dtype=dtype, ignore_frac=0.2)
     ref = O.ce_reference(logits, t, reduction="mean")
@@ -74,6 +75,20 @@ def test_ce_loss_only(dtype):
     loss, _, status = _run(logits, t, dtype, "sum", want_grad=False)
     assert status == 0
     assert_loss(loss, ref["loss"], "sum")
+
+
+@pytest.mark.parametrize("n", [1, 151, 152, 153, 1500])
+def test_ce_one_launch_row_counts(n):
+    # the single-launch form at grids below, at and above the SM count, and
+    # with more rows than threads per CTA (the in-kernel count loops)
+    logits, t = si.make_ce_logits(n, 4096, 300 + n, std=2.0, dtype="bf16", ignore_frac=0.3)
+    for reduction in ("sum", "mean"):
+        ref = O.ce_reference(logits, t, reduction=reduction)
+        loss, grad, status = _run(logits, t, "bf16", reduction)
+        assert status == 0
+        assert_loss(loss, ref["loss"], reduction)
+        if ref["n_valid"] > 0:
+            assert_grad(grad, ref["dz"], "grad_logits")
 
 
 def test_ce_out_of_range_target():
