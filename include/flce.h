@@ -211,11 +211,16 @@ size_t ce_workspace_size(int64_t N, int64_t V, int dtype, int reduction);
  *                or NULL (loss only).  Partial overlap is not allowed.
  *  target        int64 [N].
  *  ignore_index, reduction, grad_scale, grad_out_none, loss: as flce_fwd_bwd.
- *  workspace     >= ce_workspace_size(...) bytes, 256-byte aligned.
+ *  workspace     >= ce_workspace_size(...) bytes, 256-byte aligned; contents
+ *                on entry are ignored.  One workspace serves one call at a
+ *                time (calls on different streams need their own).
  *  status_dev, stream: as flce_fwd_bwd.
  *
  * Rows whose byte length is a multiple of 16 (V * sizeof(dtype)) with 16-byte
  * aligned base pointers take the vectorised path; others the scalar path.
+ * With N <= 16384 and vectorised rows of at most 144 KB the call is a single
+ * kernel launch (no separate counting pass); otherwise a small counting
+ * kernel runs first.
  */
 flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const int64_t* target,
                          int64_t N, int64_t V, int64_t ignore_index, int reduction,
