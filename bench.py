@@ -396,6 +396,17 @@ def e2e_steps(step, host, dev, steps, warmup, barrier):
         torch.cuda.synchronize()
 
     steps_pipelined(warmup)
+    # the host-to-device rate alone (one step's inputs, nothing else running),
+    # outside the timed region: it says how much of a step the copies need
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(copy)
+    with torch.cuda.stream(copy):
+        for k, v in pinned.items():
+            bufs[1][k].copy_(v, non_blocking=True)
+    e.record(copy)
+    e.synchronize()
+    h2d_ms = a.elapsed_time(e)
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -403,7 +414,7 @@ def e2e_steps(step, host, dev, steps, warmup, barrier):
     ms = (time.perf_counter() - t0) * 1e3
     barrier()
     step.dev = dev
-    return ms, h2d, d2h
+    return ms, h2d, d2h, h2d_ms
 
 
 def _device_ms(fn, steps, warmup):
@@ -739,14 +750,16 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        ms_e2e, h2d, d2h = e2e_steps(step, host, dev, max(3, args.steps // 2), 3, barrier)
-        ms_e2e /= max(3, args.steps // 2)
+        e2e_n = max(3, args.steps)
+        ms_e2e, h2d, d2h, h2d_ms = e2e_steps(step, host, dev, e2e_n, 3, barrier)
+        ms_e2e /= e2e_n
         te = torch.tensor([ms_e2e], device=device)
         if ws > 1:
             import torch.distributed as dist
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
         e2e = {"value": n * ws / (float(te.item()) / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": round(float(te.item()), 3),
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(float(te.item()), 3), "steps": e2e_n,
+               "h2d_alone_ms": round(h2d_ms, 3), "h2d_alone_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1),
                "how": "each step's inputs copied host-to-device from pinned memory on a second stream "
                       "while the previous step computes; both losses read back every step"}
 
