@@ -495,24 +495,6 @@ __device__ __forceinline__ uint4 neg_inf_vec<float>() {
   return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
 }
 
-template <typename T>
-__device__ __forceinline__ float vec_get(const uint4& v, int k) {
-  const T* e = reinterpret_cast<const T*>(&v);
-  float r = 0.f;
-#pragma unroll
-  for (int j = 0; j < 16 / static_cast<int>(sizeof(T)); ++j)
-    if (j == k) r = to_f<T>(e[j]);
-  return r;
-}
-
-template <typename T>
-__device__ __forceinline__ void vec_set(uint4& v, int k, float val) {
-  T* e = reinterpret_cast<T*>(&v);
-#pragma unroll
-  for (int j = 0; j < 16 / static_cast<int>(sizeof(T)); ++j)
-    if (j == k) e[j] = from_f<T>(val);
-}
-
 // Barrier of one thread group (named barrier `id`, `count` threads) that also
 // returns whether any of its threads passed cond = true.
 __device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool cond) {
@@ -721,13 +703,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     const int tcol = valid ? static_cast<int>(tcl) : -1;
     const int tvec = valid ? tcol / EPV : -1;
     const bool own_t = valid && (tvec % kGroupThreads) == gtid;
-    float zt = 0.f;
-    if (own_t) {
-      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
-#pragma unroll
-      for (int i = 0; i < VPT; ++i)
-        if (i == t_i) zt = vec_get<T>(v[i], t_k);
-    }
+    // the target logit straight from the ring buffer (one shared load; the
+    // buffer is not refilled before this group's barrier)
+    const float zt = own_t ? to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tcol]) : 0.f;
     // warp max, then exp(z - warp max) in place and its warp sum
     const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
     const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;  // a warp past the row's end: all -inf, sum 0
@@ -784,17 +762,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     // softmax = exp(z - warp max) * exp(warp max - M) / S: one multiply per
     // element; the target element is formed again in fp32 from its logit
     const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
-    T* grow = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
-    if (own_t) {
-      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
-      const float dt = scale * (__expf(zt - lse) - 1.f);
-#pragma unroll
-      for (int i = 0; i < VPT; ++i)
-        if (i == t_i) vec_set<T>(v[i], t_k, dt);
-    }
-    uint4* gvec = reinterpret_cast<uint4*>(grow) + gtid;
+    uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + gtid;
     if (full_rows) {
 #pragma unroll
       for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
@@ -803,6 +773,10 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       for (int i = 0; i < VPT; ++i)
         if (i * kGroupThreads + gtid < nvec) __stcs(gvec + i * kGroupThreads, v[i]);
     }
+    // the target element, formed again in fp32 from its logit, replaces what
+    // the vector store above wrote there (same thread, so it lands last)
+    if (own_t)
+      static_cast<T*>(p.grad)[static_cast<int64_t>(row) * p.V + tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
   }
   // the other group gave up: copies it would have consumed must land first
   if (gtid == 0 && *static_cast<volatile int*>(&s_abort)) drain();
@@ -926,13 +900,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     const int tcol = valid ? static_cast<int>(tcl) : -1;
     const int tvec = valid ? tcol / EPV - vbase : -1;  // the target's vector within this half
     const bool own_t = valid && tvec >= 0 && tvec < hvec && (tvec % kGroupThreads) == gtid;
-    float zt = 0.f;
-    if (own_t) {
-      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
-#pragma unroll
-      for (int i = 0; i < VPT; ++i)
-        if (i == t_i) zt = vec_get<T>(v[i], t_k);
-    }
+    // the target logit straight from this half's buffer (one shared load)
+    const float zt =
+        own_t ? to_f<T>(reinterpret_cast<const T*>(ring_smem + b * half_stride)[tcol - vbase * EPV]) : 0.f;
     const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
     const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;
     const float2 nmL = make_float2(nm, nm);
@@ -991,17 +961,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
-    if (own_t) {
-      const int t_i = tvec / kGroupThreads, t_k = tcol % EPV;
-      const float dt = scale * (__expf(zt - lse) - 1.f);
-#pragma unroll
-      for (int i = 0; i < VPT; ++i)
-        if (i == t_i) vec_set<T>(v[i], t_k, dt);
-    }
-    uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + vbase + gtid;
+    T* grow = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V;
+    uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
       if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
+    // the target element replaces what the vector store wrote there
+    if (own_t) grow[tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
   }
 
   if (p.loss_out != nullptr) {  // as in the row-ring form: the CTA's partial, then one CTA adds them
