@@ -424,9 +424,9 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
   int* status = status_dev != nullptr ? status_dev : &hdr->status;
   float* loss_rows = reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(ws + L.loss_rows);
 
-  const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned(logits, 16) &&
-                   (grad_logits == nullptr || aligned(grad_logits, 16));
-  if (N > 0 && N <= kCeSelfCountMaxRows && ce_rows_single_launch_ok(V, dtype, vec)) {
+  const bool ptrs16 = aligned(logits, 16) && (grad_logits == nullptr || aligned(grad_logits, 16));
+  const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && ptrs16;
+  if (N > 0 && N <= kCeSelfCountMaxRows && ce_rows_single_launch_ok(V, dtype, vec, ptrs16)) {
     // one launch: the row kernel counts the targets itself and finds the CTA
     // that adds the loss partials by flags, so nothing needs zeroing first
     CeParams p = {};
@@ -447,7 +447,7 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
     p.self_count = 1;
     p.done_flags = reinterpret_cast<unsigned long long*>(ws + L.flags);
     p.nonce = next_ce_nonce();
-    FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, false, stream));
+    FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, ptrs16, false, stream));
     return FLCE_OK;
   }
   if (N <= kCountSingleBlockMax) {
@@ -483,7 +483,7 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
     p.seg_len = seg;
     p.loss_out = reduction != FLCE_REDUCTION_NONE ? loss : nullptr;  // fused final reduction
     p.ticket = reinterpret_cast<unsigned int*>(&hdr->pad[1]);
-    FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, true, stream));
+    FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, ptrs16, true, stream));
   } else if (reduction != FLCE_REDUCTION_NONE) {
     FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, 0, reduction, &hdr->n_valid, loss, stream, false));
   }
@@ -661,7 +661,8 @@ flce_status_t ce_vp_partials(const void* logits, int dtype, const int64_t* targe
   if (!aligned(logits, esz) || !aligned(target, 8) || !aligned(lse_shard, 4) || !aligned(target_logit_shard, 4))
     return FLCE_ERR_MISALIGNED;
   if (N == 0) return FLCE_OK;
-  const bool vec = (static_cast<size_t>(V_shard) * esz) % 16 == 0 && aligned(logits, 16);
+  const bool ptrs16 = aligned(logits, 16);
+  const bool vec = (static_cast<size_t>(V_shard) * esz) % 16 == 0 && ptrs16;
   const int64_t cap = ce_cta_capacity(dtype, vec);
   const int64_t epv = ce_vector_elems(dtype, vec);
   int64_t cl = ceil_div(V_shard, cap);
@@ -683,7 +684,7 @@ flce_status_t ce_vp_partials(const void* logits, int dtype, const int64_t* targe
   p.lse_out = lse_shard;
   p.zt_out = target_logit_shard;
   p.v_offset = vocab_offset;
-  FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, false, stream));
+  FLCE_TRY_CUDA(launch_ce_rows(p, dtype, vec, ptrs16, false, stream));
   return FLCE_OK;
 }
 

@@ -495,6 +495,64 @@ __device__ __forceinline__ uint4 neg_inf_vec<float>() {
   return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
 }
 
+// Rows whose byte length is not a multiple of 16 (an odd vocabulary size):
+// TMA copies the 16-byte-aligned range that covers the row (offsets from the
+// 16-byte-aligned tensor start), never past the tensor's last whole 16
+// bytes; the elements of the neighbouring rows in its first and last vector
+// are masked to -inf and never stored.
+struct RowSpan {
+  uint64_t a0;  // first byte of the covering range
+  int nvr;      // vectors in the covering range
+  int nld;      // of them, loaded by TMA: nvr, or nvr - 1 at the tensor's end
+  int lead;     // elements of the previous row in vector 0
+  int tail;     // this row's elements in vector nvr - 1 (1 .. elements per vector)
+};
+
+template <typename T>
+__device__ __forceinline__ RowSpan row_span(int64_t row, uint64_t row_bytes, uint64_t tail_limit) {
+  const uint64_t sb = static_cast<uint64_t>(row) * row_bytes, eb = sb + row_bytes;
+  const uint64_t a0 = sb & ~15ull, a1 = (eb + 15) & ~15ull;
+  RowSpan r;
+  r.a0 = a0;
+  r.nvr = static_cast<int>((a1 - a0) >> 4);
+  r.nld = static_cast<int>(((a1 < tail_limit ? a1 : tail_limit) - a0) >> 4);
+  r.lead = static_cast<int>((sb & 15) / sizeof(T));
+  r.tail = (eb & 15) != 0 ? static_cast<int>((eb & 15) / sizeof(T)) : 16 / static_cast<int>(sizeof(T));
+  return r;
+}
+
+// Elements of v outside [lo, hi) become -inf.
+template <typename T>
+__device__ __forceinline__ void mask_outside(uint4& v, int lo, int hi) {
+  const uint4 ninf = neg_inf_vec<T>();
+  T* e = reinterpret_cast<T*>(&v);
+  const T* ni = reinterpret_cast<const T*>(&ninf);
+#pragma unroll
+  for (int k = 0; k < 16 / static_cast<int>(sizeof(T)); ++k)
+    if (k < lo || k >= hi) e[k] = ni[k];
+}
+
+// The first n elements of a vector read one by one from global memory (the
+// tensor's last, partial 16 bytes), the rest -inf.
+template <typename T>
+__device__ __forceinline__ uint4 load_first_elems(const T* src, int n) {
+  uint4 v = neg_inf_vec<T>();
+  T* e = reinterpret_cast<T*>(&v);
+#pragma unroll
+  for (int k = 0; k < 16 / static_cast<int>(sizeof(T)); ++k)
+    if (k < n) e[k] = src[k];
+  return v;
+}
+
+// Stores elements [lo, hi) of v one by one.
+template <typename T>
+__device__ __forceinline__ void store_elems(T* dst, const uint4& v, int lo, int hi) {
+  const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+  for (int k = 0; k < 16 / static_cast<int>(sizeof(T)); ++k)
+    if (k >= lo && k < hi) dst[k] = e[k];
+}
+
 // Barrier of one thread group (named barrier `id`, `count` threads) that also
 // returns whether any of its threads passed cond = true.
 __device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool cond) {
@@ -516,23 +574,27 @@ __device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool 
 // loaded by the caller before it requested the first rows, so that load is
 // ahead of them in the memory queue.  All threads of the CTA must call it.
 __device__ int cta_count_valid(const CeParams& p, int64_t t_first) {
-  int total = 0;
+  __shared__ int s_count;
+  if (threadIdx.x == 0) s_count = 0;
+  __syncthreads();
+  int count = 0;
   bool bad = false;
-  for (int64_t base = 0; base < p.N; base += blockDim.x) {
-    const int64_t i = base + threadIdx.x;
-    bool valid = false;
-    if (i < p.N) {
-      const int64_t t = base == 0 ? t_first : __ldg(p.target + i);
-      if (t != p.ignore_index) {
-        valid = t >= 0 && t < p.V;
-        bad |= !valid;
-      }
+  // independent loads (up to N / blockDim.x per thread), then one reduction
+#pragma unroll 4
+  for (int64_t i = threadIdx.x; i < p.N; i += blockDim.x) {
+    const int64_t t = i == threadIdx.x ? t_first : __ldg(p.target + i);
+    if (t != p.ignore_index) {
+      const bool in_range = t >= 0 && t < p.V;
+      count += in_range;
+      bad |= !in_range;
     }
-    total += __syncthreads_count(valid);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) count += __shfl_xor_sync(0xffffffffu, count, o);
+  if ((threadIdx.x & 31) == 0 && count > 0) atomicAdd(&s_count, count);
   if (__syncthreads_or(bad) && blockIdx.x == 0 && threadIdx.x == 0 && p.status != nullptr)
     atomicOr(p.status, FLCE_STATUS_BIT_TARGET_RANGE);
-  return total;
+  return s_count;
 }
 
 // Single-launch form: the arrival counter that finds the last CTA needs no
@@ -594,6 +656,12 @@ __device__ void ce_finish_loss(const CeParams& p, float part, int nv) {
   }
 }
 
+// Bytes between the ring's row buffers: a row, or for unaligned rows the
+// 16-byte-aligned range that covers it (at most 30 bytes more).
+__host__ __device__ constexpr uint32_t ring_buffer_stride(uint32_t row_bytes, bool unaligned) {
+  return unaligned ? (row_bytes + 32u + 127u) & ~127u : (row_bytes + 127u) & ~127u;
+}
+
 // Two independent groups of kGroupThreads threads share the CTA's ring and
 // take alternate rows, each synchronising on its own named barrier, so one
 // group's reductions and stores overlap the other's waits.
@@ -601,7 +669,7 @@ constexpr int kRingGroups = 2;
 constexpr int kGroupThreads = kRingThreads / kRingGroups;
 constexpr int kGroupWarps = kGroupThreads / 32;
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool UNAL>
 __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeParams p, int depth) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t ring_smem[];
@@ -615,7 +683,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   const int gtid = threadIdx.x % kGroupThreads;
   const uint32_t bar_id = 1 + grp;
   const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
-  const uint32_t buf_stride = (row_bytes + 127u) & ~127u;
+  const uint32_t buf_stride = ring_buffer_stride(row_bytes, UNAL);
+  const uint64_t tail_limit = (static_cast<uint64_t>(p.N) * row_bytes) & ~15ull;  // unaligned rows only
   // row ids fit in 32 bits: the host accepts N < 2^28
   const int stride = gridDim.x;
   const int n_rows = static_cast<int>(p.N);
@@ -643,9 +712,16 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   auto issue = [&](int bi, int row) {
     volatile int* cnt = s_issued;
     cnt[bi] = cnt[bi] + 1;
-    mbar_arrive_expect_tx(smem_addr(&full[bi]), row_bytes);
-    bulk_load(ring_base + bi * buf_stride, static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.V, row_bytes,
-              smem_addr(&full[bi]));
+    if constexpr (UNAL) {
+      const RowSpan sp = row_span<T>(row, row_bytes, tail_limit);
+      const uint32_t bytes = static_cast<uint32_t>(sp.nld) * 16u;
+      mbar_arrive_expect_tx(smem_addr(&full[bi]), bytes);
+      bulk_load(ring_base + bi * buf_stride, static_cast<const uint8_t*>(p.logits) + sp.a0, bytes, smem_addr(&full[bi]));
+    } else {
+      mbar_arrive_expect_tx(smem_addr(&full[bi]), row_bytes);
+      bulk_load(ring_base + bi * buf_stride, static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.V,
+                row_bytes, smem_addr(&full[bi]));
+    }
   };
   // waits (bounded) for the latest copy issued into every buffer
   auto drain = [&]() {
@@ -660,7 +736,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     for (int i = 0; i < first && i < mine; ++i) issue(i, blockIdx.x + i * stride);
     if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
   }
-  const bool full_rows = nvec == VPT * kGroupThreads;  // no vector past the row's end
+  const bool full_rows = !UNAL && nvec == VPT * kGroupThreads;  // no vector past the row's end
   int nv = 1;
   if (p.self_count) {
     nv = cta_count_valid(p, t_first);  // while the first rows load
@@ -687,7 +763,22 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     // sum and are not stored, so the row's work below needs no per-vector branch
     uint4 v[VPT];
     const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * buf_stride);
-    if (full_rows) {
+    RowSpan sp = {0, 0, 0, 0, EPV};  // unaligned rows only
+    if constexpr (UNAL) {
+      sp = row_span<T>(row, row_bytes, tail_limit);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int vi = i * kGroupThreads + gtid;
+        if (vi < sp.nld)
+          v[i] = sbuf[vi];
+        else if (vi < sp.nvr)  // the tensor's last partial 16 bytes
+          v[i] = load_first_elems<T>(
+              reinterpret_cast<const T*>(static_cast<const uint8_t*>(p.logits) + sp.a0 + 16ull * vi), sp.tail);
+        else
+          v[i] = neg_inf_vec<T>();
+        if (vi == 0 || vi == sp.nvr - 1) mask_outside<T>(v[i], vi == 0 ? sp.lead : 0, vi == sp.nvr - 1 ? sp.tail : EPV);
+      }
+    } else if (full_rows) {
 #pragma unroll
       for (int i = 0; i < VPT; ++i) v[i] = sbuf[i * kGroupThreads + gtid];
     } else {
@@ -701,11 +792,19 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     const int64_t tcl = t - p.v_offset;
     const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
     const int tcol = valid ? static_cast<int>(tcl) : -1;
-    const int tvec = valid ? tcol / EPV : -1;
+    const int tel = valid ? (UNAL ? sp.lead : 0) + tcol : -1;  // its element in the buffer
+    const int tvec = valid ? tel / EPV : -1;
     const bool own_t = valid && (tvec % kGroupThreads) == gtid;
     // the target logit straight from the ring buffer (one shared load; the
-    // buffer is not refilled before this group's barrier)
-    const float zt = own_t ? to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tcol]) : 0.f;
+    // buffer is not refilled before this group's barrier), or from global
+    // memory in the tensor's last partial 16 bytes
+    float zt = 0.f;
+    if (own_t) {
+      if (!UNAL || tvec < sp.nld)
+        zt = to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tel]);
+      else
+        zt = to_f<T>(static_cast<const T*>(p.logits)[static_cast<int64_t>(row) * p.V + tcol]);
+    }
     // warp max, then exp(z - warp max) in place and its warp sum
     const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
     const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;  // a warp past the row's end: all -inf, sum 0
@@ -764,14 +863,28 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
-    uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + gtid;
-    if (full_rows) {
+    if constexpr (UNAL) {
+      uint8_t* gb = static_cast<uint8_t*>(p.grad) + sp.a0;
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
+      for (int i = 0; i < VPT; ++i) {
+        const int vi = i * kGroupThreads + gtid;
+        if (vi >= sp.nvr) continue;
+        const int lo = vi == 0 ? sp.lead : 0, hi = vi == sp.nvr - 1 ? sp.tail : EPV;
+        if (lo > 0 || hi < EPV)  // a vector shared with a neighbouring row: this row's elements only
+          store_elems<T>(reinterpret_cast<T*>(gb + 16ull * vi), v[i], lo, hi);
+        else
+          __stcs(reinterpret_cast<uint4*>(gb + 16ull * vi), v[i]);
+      }
     } else {
+      uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + gtid;
+      if (full_rows) {
 #pragma unroll
-      for (int i = 0; i < VPT; ++i)
-        if (i * kGroupThreads + gtid < nvec) __stcs(gvec + i * kGroupThreads, v[i]);
+        for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+          if (i * kGroupThreads + gtid < nvec) __stcs(gvec + i * kGroupThreads, v[i]);
+      }
     }
     // the target element, formed again in fp32 from its logit, replaces what
     // the vector store above wrote there (same thread, so it lands last)
@@ -791,13 +904,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   }
 }
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool UNAL>
 cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, bool pdl, cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(ce_rows_ring_kernel<T, VPT>,
+    const cudaError_t e = cudaFuncSetAttribute(ce_rows_ring_kernel<T, VPT, UNAL>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kRingSmemBudget + 1024));
     if (e != cudaSuccess) return e;
@@ -814,7 +927,7 @@ cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, b
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   CeParams pc = p;
-  return cudaLaunchKernelEx(&cfg, ce_rows_ring_kernel<T, VPT>, pc, depth);
+  return cudaLaunchKernelEx(&cfg, ce_rows_ring_kernel<T, VPT, UNAL>, pc, depth);
 }
 
 // Half-row ring form, for rows of 72-144 KB (fp32 logits up to V = 36864,
@@ -841,6 +954,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
   const int hvec0 = static_cast<int>(half_bytes / 16);                 // vectors in the first half
   const int hvec = grp == 0 ? hvec0 : nvec - hvec0;                     // vectors in this group's half
   const int vbase = grp == 0 ? 0 : hvec0;                               // its first vector in the row
+  const bool full_half = hvec == VPT * kGroupThreads;                   // no vector past the half's end
   const int stride = gridDim.x;
   const int n_rows = static_cast<int>(p.N);
   const int mine = n_rows > static_cast<int>(blockIdx.x) ? (n_rows - 1 - static_cast<int>(blockIdx.x)) / stride + 1 : 0;
@@ -890,10 +1004,15 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     const bool ok = mbar_wait_sleep(smem_addr(&full[b]), static_cast<uint32_t>((s / 3) & 1), ctl);
     uint4 v[VPT];
     const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * half_stride);
+    if (full_half) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int vi = i * kGroupThreads + gtid;
-      v[i] = vi < hvec ? sbuf[vi] : neg_inf_vec<T>();
+      for (int i = 0; i < VPT; ++i) v[i] = sbuf[i * kGroupThreads + gtid];
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int vi = i * kGroupThreads + gtid;
+        v[i] = vi < hvec ? sbuf[vi] : neg_inf_vec<T>();
+      }
     }
     const int64_t tcl = t - p.v_offset;
     const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
@@ -963,9 +1082,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
     T* grow = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V;
     uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
+    if (full_half) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i)
-      if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
+      for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
+    }
     // the target element replaces what the vector store wrote there
     if (own_t) grow[tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
   }
@@ -1034,50 +1158,66 @@ int64_t ce_vector_elems(int dtype, bool vector_path) {
   return vector_path ? (dtype == FLCE_DTYPE_FP32 ? 4 : 8) : 1;
 }
 
-bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path) {
+// Rows that are not a whole number of 16-byte vectors go to the row-ring
+// form too when both pointers are 16-byte aligned and a row has at least 32
+// bytes (its covering range then always holds a whole vector TMA can load).
+static bool ce_unaligned_ring_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
   const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  return vector_path && row_bytes <= 144 * 1024 && device_sm_count() <= kCeMaxFlags;
+  return !vector_path && aligned_ptrs && row_bytes >= 32 && row_bytes <= 72 * 1024;
+}
+
+bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
+  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
+  return ((vector_path && row_bytes <= 144 * 1024) || ce_unaligned_ring_ok(V, dtype, vector_path, aligned_ptrs)) &&
+         device_sm_count() <= kCeMaxFlags;
 }
 
 // Row-ring form when rows fit (see above); 0 when it does not apply.
-int ce_ring_depth(int64_t V, int dtype, bool vector_path) {
-  if (!vector_path) return 0;
+int ce_ring_depth(int64_t V, int dtype, bool vector_path, bool unaligned) {
+  if (!vector_path && !unaligned) return 0;
   const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  const int64_t stride = (row_bytes + 127) / 128 * 128;
   if (row_bytes > 72 * 1024) return 0;
-  int64_t depth = kRingSmemBudget / stride;
+  int64_t depth = kRingSmemBudget / ring_buffer_stride(static_cast<uint32_t>(row_bytes), unaligned);
   if (depth > kRingMaxDepth) depth = kRingMaxDepth;
   return depth >= 2 ? static_cast<int>(depth) : 0;
 }
 
-cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool pdl, cudaStream_t s) {
+template <bool UNAL>
+static cudaError_t launch_ring(const CeParams& p, int dtype, int depth, int vpt, int grid, size_t smem, bool pdl,
+                               cudaStream_t s) {
+  if (dtype == FLCE_DTYPE_BF16)
+    return vpt <= 2   ? launch_ring_t<uint16_t, 2, UNAL>(p, depth, grid, smem, pdl, s)
+           : vpt <= 4 ? launch_ring_t<uint16_t, 4, UNAL>(p, depth, grid, smem, pdl, s)
+           : vpt <= 8 ? launch_ring_t<uint16_t, 8, UNAL>(p, depth, grid, smem, pdl, s)
+                      : launch_ring_t<uint16_t, 10, UNAL>(p, depth, grid, smem, pdl, s);
+  if (dtype == FLCE_DTYPE_FP16)
+    return vpt <= 2   ? launch_ring_t<__half, 2, UNAL>(p, depth, grid, smem, pdl, s)
+           : vpt <= 4 ? launch_ring_t<__half, 4, UNAL>(p, depth, grid, smem, pdl, s)
+           : vpt <= 8 ? launch_ring_t<__half, 8, UNAL>(p, depth, grid, smem, pdl, s)
+                      : launch_ring_t<__half, 10, UNAL>(p, depth, grid, smem, pdl, s);
+  return vpt <= 2   ? launch_ring_t<float, 2, UNAL>(p, depth, grid, smem, pdl, s)
+         : vpt <= 4 ? launch_ring_t<float, 4, UNAL>(p, depth, grid, smem, pdl, s)
+         : vpt <= 8 ? launch_ring_t<float, 8, UNAL>(p, depth, grid, smem, pdl, s)
+                    : launch_ring_t<float, 10, UNAL>(p, depth, grid, smem, pdl, s);
+}
+
+cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool aligned_ptrs, bool pdl,
+                           cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
   prof_begin(s, FLCE_KERNEL_CE_ROWS);
   cudaError_t e;
-  const int depth = ce_ring_depth(p.V, dtype, vector_path);
+  const bool unal = ce_unaligned_ring_ok(p.V, dtype, vector_path, aligned_ptrs);
+  const int depth = ce_ring_depth(p.V, dtype, vector_path, unal);
   if (depth > 0) {
     const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-    const int64_t vecs = row_bytes / 16;
+    // vectors a thread may hold: the row's, or those of its covering range
+    const int64_t vecs = unal ? (row_bytes + 14 + 15) / 16 : row_bytes / 16;
     const int vpt = static_cast<int>((vecs + kGroupThreads - 1) / kGroupThreads);
-    const size_t smem = static_cast<size_t>(depth) * ((row_bytes + 127) / 128 * 128);
+    const size_t smem = static_cast<size_t>(depth) * ring_buffer_stride(static_cast<uint32_t>(row_bytes), unal);
     int grid = device_sm_count();
     if (grid > p.N) grid = static_cast<int>(p.N);
-    if (dtype == FLCE_DTYPE_BF16) {
-      e = vpt <= 2   ? launch_ring_t<uint16_t, 2>(p, depth, grid, smem, pdl, s)
-          : vpt <= 4 ? launch_ring_t<uint16_t, 4>(p, depth, grid, smem, pdl, s)
-          : vpt <= 8 ? launch_ring_t<uint16_t, 8>(p, depth, grid, smem, pdl, s)
-                     : launch_ring_t<uint16_t, 10>(p, depth, grid, smem, pdl, s);
-    } else if (dtype == FLCE_DTYPE_FP16) {
-      e = vpt <= 2   ? launch_ring_t<__half, 2>(p, depth, grid, smem, pdl, s)
-          : vpt <= 4 ? launch_ring_t<__half, 4>(p, depth, grid, smem, pdl, s)
-          : vpt <= 8 ? launch_ring_t<__half, 8>(p, depth, grid, smem, pdl, s)
-                     : launch_ring_t<__half, 10>(p, depth, grid, smem, pdl, s);
-    } else {
-      e = vpt <= 2   ? launch_ring_t<float, 2>(p, depth, grid, smem, pdl, s)
-          : vpt <= 4 ? launch_ring_t<float, 4>(p, depth, grid, smem, pdl, s)
-          : vpt <= 8 ? launch_ring_t<float, 8>(p, depth, grid, smem, pdl, s)
-                     : launch_ring_t<float, 10>(p, depth, grid, smem, pdl, s);
-    }
+    e = unal ? launch_ring<true>(p, dtype, depth, vpt, grid, smem, pdl, s)
+             : launch_ring<false>(p, dtype, depth, vpt, grid, smem, pdl, s);
     prof_end(s);
     return e;
   }

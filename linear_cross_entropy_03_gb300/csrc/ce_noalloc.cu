@@ -88,8 +88,8 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
       cudaSuccess)
     return FLCE_ERR_CUDA;
   if (N > 0) {
-    const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && aligned_to(logits, 16) &&
-                     (grad_logits == nullptr || aligned_to(grad_logits, 16));
+    const bool ptrs16 = aligned_to(logits, 16) && (grad_logits == nullptr || aligned_to(grad_logits, 16));
+    const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && ptrs16;
     const int64_t cap = ce_cta_capacity(dtype, vec);
     const int64_t epv = ce_vector_elems(dtype, vec);
     int64_t cl = ceil_div64(V, cap);
@@ -111,7 +111,7 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
     p.status = status;
     p.cluster = static_cast<int>(cl);
     p.seg_len = seg;
-    if (launch_ce_rows(p, dtype, vec, true, stream) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (launch_ce_rows(p, dtype, vec, ptrs16, true, stream) != cudaSuccess) return FLCE_ERR_CUDA;
   }
   if (reduction != FLCE_REDUCTION_NONE &&
       launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, N > 0) != cudaSuccess)

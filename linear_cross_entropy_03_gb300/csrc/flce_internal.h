@@ -179,10 +179,13 @@ cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction,
                                float* loss, cudaStream_t s, bool pdl);
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
-cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool pdl, cudaStream_t s);
+// vector_path: rows are whole 16-byte vectors and both pointers 16-byte
+// aligned; aligned_ptrs: both pointers 16-byte aligned (rows of any length).
+cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool aligned_ptrs, bool pdl,
+                           cudaStream_t s);
 // Whether rows of V elements go to a form that supports the single launch
 // (the row-ring or half-row kernel), and at most how many CTAs it launches.
-bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path);
+bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 
 int gemm_max_smem_ok();  // sets kernel attributes once per device; 0 on failure

@@ -91,6 +91,24 @@ def test_ce_one_launch_row_counts(n):
             assert_grad(grad, ref["dz"], "grad_logits")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("n,v", [(7, 17), (300, 1001), (153, 30001), (100, 9999), (64, 4097), (5, 18431)])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_ce_rows_not_whole_vectors(dtype, n, v, in_place):
+    # rows whose byte length is not a multiple of 16: the row-ring kernel loads
+    # each row's 16-byte-aligned covering range, masks the neighbours' elements
+    # and stores only its own (in place, a neighbour's gradient must survive)
+    logits, t = si.make_ce_logits(n, v, 400 + n + v, std=2.0, dtype=dtype, ignore_frac=0.1)
+    for reduction in ("none", "mean"):
+        go = si.make_grad_out(n, 5) if reduction == "none" else None
+        ref = O.ce_reference(logits, t, reduction=reduction, grad_out=go)
+        loss, grad, status = _run(logits, t, dtype, reduction, in_place=in_place, grad_out=go)
+        assert status == 0
+        assert_loss(loss, ref["loss"], reduction)
+        assert_grad(grad, ref["dz"], "grad_logits")
+        assert np.all(grad[~ref["valid"]] == 0.0)
+
+
 def test_ce_out_of_range_target():
     logits, t = si.make_ce_logits(50, 300, 6)
     t[4] = 300
