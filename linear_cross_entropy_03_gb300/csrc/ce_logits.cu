@@ -937,7 +937,7 @@ cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, b
 // the two halves' partials, and each group writes its half's gradient.
 // Thread 0 keeps three half-rows in flight: after row j's barrier it
 // requests the second half of row j + 1 and the first half of row j + 2.
-template <typename T, int VPT>
+template <typename T, int VPT, bool UNAL>
 __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeParams p, uint32_t half_bytes) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t ring_smem[];
@@ -952,9 +952,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
   const uint32_t half_stride = (half_bytes + 127u) & ~127u;
   const int nvec = static_cast<int>(row_bytes / 16);
   const int hvec0 = static_cast<int>(half_bytes / 16);                 // vectors in the first half
-  const int hvec = grp == 0 ? hvec0 : nvec - hvec0;                     // vectors in this group's half
+  // unaligned rows: the halves split the row's 16-byte-aligned covering
+  // range, whose length varies by row (group 1's half is set per row)
+  const uint64_t tail_limit = (static_cast<uint64_t>(p.N) * row_bytes) & ~15ull;
+  int hvec = grp == 0 ? hvec0 : nvec - hvec0;                           // vectors in this group's half
   const int vbase = grp == 0 ? 0 : hvec0;                               // its first vector in the row
-  const bool full_half = hvec == VPT * kGroupThreads;                   // no vector past the half's end
+  const bool full_half = !UNAL && hvec == VPT * kGroupThreads;          // no vector past the half's end
   const int stride = gridDim.x;
   const int n_rows = static_cast<int>(p.N);
   const int mine = n_rows > static_cast<int>(blockIdx.x) ? (n_rows - 1 - static_cast<int>(blockIdx.x)) / stride + 1 : 0;
@@ -975,12 +978,20 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     const int j = s >> 1, h = s & 1;
     if (j >= mine) return;
     const int row = blockIdx.x + j * stride;
-    const uint32_t bytes = h == 0 ? half_bytes : row_bytes - half_bytes;
     const uint32_t b = static_cast<uint32_t>(s % 3);
+    uint64_t src;
+    uint32_t bytes;
+    if constexpr (UNAL) {
+      const RowSpan sp = row_span<T>(row, row_bytes, tail_limit);
+      src = sp.a0 + (h ? half_bytes : 0u);
+      bytes = h == 0 ? half_bytes : static_cast<uint32_t>(sp.nld) * 16u - half_bytes;
+    } else {
+      src = static_cast<uint64_t>(row) * row_bytes + (h ? half_bytes : 0u);
+      bytes = h == 0 ? half_bytes : row_bytes - half_bytes;
+    }
     mbar_arrive_expect_tx(smem_addr(&full[b]), bytes);
-    bulk_load(ring_base + b * half_stride,
-              reinterpret_cast<const uint8_t*>(p.logits) + static_cast<int64_t>(row) * row_bytes + (h ? half_bytes : 0),
-              bytes, smem_addr(&full[b]));
+    bulk_load(ring_base + b * half_stride, reinterpret_cast<const uint8_t*>(p.logits) + src, bytes,
+              smem_addr(&full[b]));
   };
   const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
   if (threadIdx.x == 0) {
@@ -1004,7 +1015,25 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     const bool ok = mbar_wait_sleep(smem_addr(&full[b]), static_cast<uint32_t>((s / 3) & 1), ctl);
     uint4 v[VPT];
     const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * half_stride);
-    if (full_half) {
+    RowSpan sp = {0, 0, 0, 0, EPV};  // unaligned rows only
+    if constexpr (UNAL) {
+      sp = row_span<T>(row, row_bytes, tail_limit);
+      if (grp == 1) hvec = sp.nvr - hvec0;
+      const int loaded = grp == 0 ? hvec0 : sp.nld - hvec0;  // vectors of this half in the buffer
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int vi = i * kGroupThreads + gtid, va = vbase + vi;  // in the half, in the covering range
+        if (vi < loaded)
+          v[i] = sbuf[vi];
+        else if (vi < hvec)  // the tensor's last partial 16 bytes
+          v[i] = load_first_elems<T>(
+              reinterpret_cast<const T*>(static_cast<const uint8_t*>(p.logits) + sp.a0 + 16ull * va), sp.tail);
+        else
+          v[i] = neg_inf_vec<T>();
+        if (vi < hvec && (va == 0 || va == sp.nvr - 1))
+          mask_outside<T>(v[i], va == 0 ? sp.lead : 0, va == sp.nvr - 1 ? sp.tail : EPV);
+      }
+    } else if (full_half) {
 #pragma unroll
       for (int i = 0; i < VPT; ++i) v[i] = sbuf[i * kGroupThreads + gtid];
     } else {
@@ -1017,11 +1046,18 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
     const int64_t tcl = t - p.v_offset;
     const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
     const int tcol = valid ? static_cast<int>(tcl) : -1;
-    const int tvec = valid ? tcol / EPV - vbase : -1;  // the target's vector within this half
+    const int tel = valid ? (UNAL ? sp.lead : 0) + tcol : -1;  // its element in the (covering) row
+    const int tvec = valid ? tel / EPV - vbase : -1;           // the target's vector within this half
     const bool own_t = valid && tvec >= 0 && tvec < hvec && (tvec % kGroupThreads) == gtid;
-    // the target logit straight from this half's buffer (one shared load)
-    const float zt =
-        own_t ? to_f<T>(reinterpret_cast<const T*>(ring_smem + b * half_stride)[tcol - vbase * EPV]) : 0.f;
+    // the target logit straight from this half's buffer (one shared load), or
+    // from global memory in the tensor's last partial 16 bytes
+    float zt = 0.f;
+    if (own_t) {
+      if (!UNAL || vbase + tvec < sp.nld)
+        zt = to_f<T>(reinterpret_cast<const T*>(ring_smem + b * half_stride)[tel - vbase * EPV]);
+      else
+        zt = to_f<T>(static_cast<const T*>(p.logits)[static_cast<int64_t>(row) * p.V + tcol]);
+    }
     const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
     const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;
     const float2 nmL = make_float2(nm, nm);
@@ -1081,11 +1117,24 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
 #pragma unroll
     for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
     T* grow = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V;
-    uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
-    if (full_half) {
+    if constexpr (UNAL) {
+      uint8_t* gb = static_cast<uint8_t*>(p.grad) + sp.a0;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int vi = i * kGroupThreads + gtid, va = vbase + vi;
+        if (vi >= hvec) continue;
+        const int lo = va == 0 ? sp.lead : 0, hi = va == sp.nvr - 1 ? sp.tail : EPV;
+        if (lo > 0 || hi < EPV)  // a vector shared with a neighbouring row: this row's elements only
+          store_elems<T>(reinterpret_cast<T*>(gb + 16ull * va), v[i], lo, hi);
+        else
+          __stcs(reinterpret_cast<uint4*>(gb + 16ull * va), v[i]);
+      }
+    } else if (full_half) {
+      uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
     } else {
+      uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
 #pragma unroll
       for (int i = 0; i < VPT; ++i)
         if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
@@ -1100,13 +1149,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeP
   }
 }
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool UNAL>
 cudaError_t launch_half_t(const CeParams& p, uint32_t half_bytes, int grid, bool pdl, cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(ce_rows_half_kernel<T, VPT>,
+    const cudaError_t e = cudaFuncSetAttribute(ce_rows_half_kernel<T, VPT, UNAL>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kRingSmemBudget + 1024));
     if (e != cudaSuccess) return e;
@@ -1123,7 +1172,7 @@ cudaError_t launch_half_t(const CeParams& p, uint32_t half_bytes, int grid, bool
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   CeParams pc = p;
-  return cudaLaunchKernelEx(&cfg, ce_rows_half_kernel<T, VPT>, pc, half_bytes);
+  return cudaLaunchKernelEx(&cfg, ce_rows_half_kernel<T, VPT, UNAL>, pc, half_bytes);
 }
 
 template <typename T, int EPV>
@@ -1166,9 +1215,17 @@ static bool ce_unaligned_ring_ok(int64_t V, int dtype, bool vector_path, bool al
   return !vector_path && aligned_ptrs && row_bytes >= 32 && row_bytes <= 72 * 1024;
 }
 
+// Rows of 72-144 KB: the half-row form, for whole-vector rows and, with
+// 16-byte-aligned pointers, for the others.
+static bool ce_half_rows_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
+  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
+  return (vector_path || aligned_ptrs) && row_bytes > 72 * 1024 && row_bytes <= 144 * 1024;
+}
+
 bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
   const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  return ((vector_path && row_bytes <= 144 * 1024) || ce_unaligned_ring_ok(V, dtype, vector_path, aligned_ptrs)) &&
+  return ((vector_path && row_bytes <= 144 * 1024) || ce_unaligned_ring_ok(V, dtype, vector_path, aligned_ptrs) ||
+          ce_half_rows_ok(V, dtype, vector_path, aligned_ptrs)) &&
          device_sm_count() <= kCeMaxFlags;
 }
 
@@ -1180,6 +1237,19 @@ int ce_ring_depth(int64_t V, int dtype, bool vector_path, bool unaligned) {
   int64_t depth = kRingSmemBudget / ring_buffer_stride(static_cast<uint32_t>(row_bytes), unaligned);
   if (depth > kRingMaxDepth) depth = kRingMaxDepth;
   return depth >= 2 ? static_cast<int>(depth) : 0;
+}
+
+template <bool UNAL>
+static cudaError_t launch_half(const CeParams& p, int dtype, int vpt, uint32_t half_bytes, int grid, bool pdl,
+                               cudaStream_t s) {
+  if (dtype == FLCE_DTYPE_BF16)
+    return vpt <= 8 ? launch_half_t<uint16_t, 8, UNAL>(p, half_bytes, grid, pdl, s)
+                    : launch_half_t<uint16_t, 10, UNAL>(p, half_bytes, grid, pdl, s);
+  if (dtype == FLCE_DTYPE_FP16)
+    return vpt <= 8 ? launch_half_t<__half, 8, UNAL>(p, half_bytes, grid, pdl, s)
+                    : launch_half_t<__half, 10, UNAL>(p, half_bytes, grid, pdl, s);
+  return vpt <= 8 ? launch_half_t<float, 8, UNAL>(p, half_bytes, grid, pdl, s)
+                  : launch_half_t<float, 10, UNAL>(p, half_bytes, grid, pdl, s);
 }
 
 template <bool UNAL>
@@ -1221,22 +1291,17 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
     prof_end(s);
     return e;
   }
-  // rows of 72-144 KB: the half-row ring form
+  // rows of 72-144 KB: the half-row ring form (rows that are not whole
+  // vectors: the halves split their 16-byte-aligned covering range)
   const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  if (vector_path && row_bytes > 72 * 1024 && row_bytes <= 144 * 1024) {
-    const uint32_t half_bytes = static_cast<uint32_t>((row_bytes / 16 + 1) / 2 * 16);
+  if (ce_half_rows_ok(p.V, dtype, vector_path, aligned_ptrs)) {
+    const int64_t vecs = vector_path ? row_bytes / 16 : (row_bytes + 14 + 15) / 16;
+    const uint32_t half_bytes = static_cast<uint32_t>((vecs + 1) / 2 * 16);
     const int vpt = static_cast<int>((half_bytes / 16 + kGroupThreads - 1) / kGroupThreads);
     int grid = device_sm_count();
     if (grid > p.N) grid = static_cast<int>(p.N);
-    if (dtype == FLCE_DTYPE_BF16)
-      e = vpt <= 8 ? launch_half_t<uint16_t, 8>(p, half_bytes, grid, pdl, s)
-                   : launch_half_t<uint16_t, 10>(p, half_bytes, grid, pdl, s);
-    else if (dtype == FLCE_DTYPE_FP16)
-      e = vpt <= 8 ? launch_half_t<__half, 8>(p, half_bytes, grid, pdl, s)
-                   : launch_half_t<__half, 10>(p, half_bytes, grid, pdl, s);
-    else
-      e = vpt <= 8 ? launch_half_t<float, 8>(p, half_bytes, grid, pdl, s)
-                   : launch_half_t<float, 10>(p, half_bytes, grid, pdl, s);
+    e = vector_path ? launch_half<false>(p, dtype, vpt, half_bytes, grid, pdl, s)
+                    : launch_half<true>(p, dtype, vpt, half_bytes, grid, pdl, s);
     prof_end(s);
     return e;
   }

@@ -92,12 +92,14 @@ def test_ce_one_launch_row_counts(n):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-@pytest.mark.parametrize("n,v", [(7, 17), (300, 1001), (153, 30001), (100, 9999), (64, 4097), (5, 18431)])
+@pytest.mark.parametrize("n,v", [(7, 17), (300, 1001), (153, 30001), (100, 9999), (64, 4097), (5, 18431),
+                                 (40, 50257), (9, 36867), (20, 20001), (11, 32001)])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_ce_rows_not_whole_vectors(dtype, n, v, in_place):
-    # rows whose byte length is not a multiple of 16: the row-ring kernel loads
-    # each row's 16-byte-aligned covering range, masks the neighbours' elements
-    # and stores only its own (in place, a neighbour's gradient must survive)
+    # rows whose byte length is not a multiple of 16: the row-ring and
+    # half-row kernels load each row's 16-byte-aligned covering range, mask the
+    # neighbours' elements and store only their own (in place, a neighbour's
+    # gradient must survive)
     logits, t = si.make_ce_logits(n, v, 400 + n + v, std=2.0, dtype=dtype, ignore_frac=0.1)
     for reduction in ("none", "mean"):
         go = si.make_grad_out(n, 5) if reduction == "none" else None
