@@ -930,6 +930,197 @@ cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, b
   return cudaLaunchKernelEx(&cfg, ce_rows_ring_kernel<T, VPT, UNAL>, pc, depth);
 }
 
+// Streaming form, for rows over 144 KB (16-bit V > 73728, fp32 V > 36864),
+// too long for one SM to hold: persistent 512-thread CTAs, two per SM, take
+// rows blockIdx.x, blockIdx.x + gridDim.x, ...; per row, pass 1 reads the row
+// from DRAM in steps of 8 vectors per thread, keeping a per-thread online
+// (max, sum of exp), and the CTA combines them into the LSE; pass 2 reads
+// the row again (an L2 hit: the rows in flight on all SMs take well under
+// L2's capacity) and writes the gradient.  DRAM moves each logit once each
+// way; the exponentials are computed twice.  Rows that are not whole
+// 16-byte vectors use their 16-byte-aligned covering range, masked as in the
+// ring forms.
+constexpr int kStreamThreads = 512;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamU = 8;  // vectors per thread per step
+
+template <typename T, bool UNAL>
+__device__ __forceinline__ void stream_load(uint4 (&v)[kStreamU], const uint8_t* logits, const RowSpan& sp, int base,
+                                            bool last_use) {
+  constexpr int EPV = 16 / sizeof(T);
+  const uint4* src = reinterpret_cast<const uint4*>(logits + sp.a0);
+#pragma unroll
+  for (int i = 0; i < kStreamU; ++i) {
+    const int vi = base + i * kStreamThreads + static_cast<int>(threadIdx.x);
+    if (vi < sp.nld)
+      v[i] = last_use ? __ldcs(src + vi) : src[vi];
+    else if (UNAL && vi < sp.nvr)  // the tensor's last partial 16 bytes
+      v[i] = load_first_elems<T>(reinterpret_cast<const T*>(logits + sp.a0 + 16ull * vi), sp.tail);
+    else
+      v[i] = neg_inf_vec<T>();
+    if (UNAL && vi < sp.nvr && (vi == 0 || vi == sp.nvr - 1))
+      mask_outside<T>(v[i], vi == 0 ? sp.lead : 0, vi == sp.nvr - 1 ? sp.tail : EPV);
+  }
+}
+
+template <typename T, bool UNAL>
+__global__ void __launch_bounds__(kStreamThreads, 2) ce_rows_stream_kernel(const CeParams p) {
+  constexpr int EPV = 16 / sizeof(T);
+  __shared__ float2 s_part[2][kStreamWarps];  // per warp (max, sum of exp), by row parity
+  __shared__ float s_gsum, s_gcomp;           // compensated sum of the CTA's row losses
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t row_bytes = static_cast<uint64_t>(p.V) * sizeof(T);
+  const uint64_t tail_limit = (static_cast<uint64_t>(p.N) * row_bytes) & ~15ull;
+  const uint8_t* logits = static_cast<const uint8_t*>(p.logits);
+  const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
+  if (threadIdx.x == 0) {
+    s_gsum = s_gcomp = 0.f;
+    if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+  }
+  int nv = 1;
+  if (p.self_count) {
+    nv = cta_count_valid(p, t_first);  // (its barriers also publish the zeroed sums)
+  } else {
+    grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
+    if (p.reduction == FLCE_REDUCTION_MEAN) nv = *p.n_valid;
+    __syncthreads();
+  }
+
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.N; row += gridDim.x, parity ^= 1) {
+    RowSpan sp;
+    if constexpr (UNAL) {
+      sp = row_span<T>(row, row_bytes, tail_limit);
+    } else {
+      sp.a0 = static_cast<uint64_t>(row) * row_bytes;
+      sp.nvr = sp.nld = static_cast<int>(row_bytes / 16);
+      sp.lead = 0;
+      sp.tail = EPV;
+    }
+    const int64_t t = __ldg(p.target + row);
+    const float go = p.grad_out != nullptr ? __ldg(p.grad_out + row) : 1.f;
+    const int64_t tcl = t - p.v_offset;
+    const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
+    const int tcol = valid ? static_cast<int>(tcl) : -1;
+    const int tvec = valid ? (sp.lead + tcol) / EPV : -1;
+    const bool own_t = valid && (tvec % kStreamThreads) == static_cast<int>(threadIdx.x);
+    // the target logit, read before anything of the row is overwritten
+    const float zt = own_t ? to_f<T>(static_cast<const T*>(p.logits)[row * p.V + tcol]) : 0.f;
+
+    // pass 1: online (max, sum of exp(z - max)) per thread
+    float m = -INFINITY, sum = 0.f;
+    for (int base = 0; base < sp.nvr; base += kStreamThreads * kStreamU) {
+      uint4 v[kStreamU];
+      stream_load<T, UNAL>(v, logits, sp, base, false);
+      const float cm = vec_max_all<T, kStreamU>(v, kStreamU, 1);
+      if (cm > m) {
+        sum = m > -INFINITY ? sum * ex2_approx((m - cm) * kLog2e) : 0.f;
+        m = cm;
+      }
+      if (m > -INFINITY) {
+        const float nm = -m * kLog2e;
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kStreamU; ++i) vec_exp_acc<T>(v[i], make_float2(nm, nm), acc);
+        sum += acc.x + acc.y;
+      }
+    }
+    // warp, then CTA combine of the (max, sum) pairs
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      const float mm = fmaxf(m, m2);
+      if (mm > -INFINITY) {
+        sum = (m > -INFINITY ? sum * ex2_approx((m - mm) * kLog2e) : 0.f) +
+              (m2 > -INFINITY ? s2 * ex2_approx((m2 - mm) * kLog2e) : 0.f);
+        m = mm;
+      }
+    }
+    if (lane == 0) s_part[parity][warp] = make_float2(m, sum);
+    __syncthreads();  // one barrier per row: the partials of row parity p are rewritten two rows later
+    const float2 q = lane < kStreamWarps ? s_part[parity][lane] : make_float2(-INFINITY, 0.f);
+    const float M = warp_max(q.x);
+    const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
+    const float lse = M + logf(S);
+
+    if (p.lse_out != nullptr) {  // partials of a vocabulary shard
+      if (own_t) p.zt_out[row] = zt;
+      if (threadIdx.x == 0) {
+        p.lse_out[row] = lse;
+        if (!valid) p.zt_out[row] = 0.f;
+      }
+      continue;
+    }
+    if (p.loss_out != nullptr) {  // the CTA's rows' losses in row order (ordered by the barriers)
+      if (own_t) {
+        const float y = (lse - zt) - s_gcomp;
+        const float t2 = s_gsum + y;
+        s_gcomp = (t2 - s_gsum) - y;
+        s_gsum = t2;
+      }
+    } else {
+      if (own_t) p.loss_rows[row] = lse - zt;
+      if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
+    }
+    if (p.grad == nullptr) continue;
+    float scale = 0.f;
+    if (valid) {
+      if (p.reduction == FLCE_REDUCTION_MEAN)
+        scale = p.grad_scale / static_cast<float>(nv);
+      else if (p.reduction == FLCE_REDUCTION_SUM)
+        scale = p.grad_scale;
+      else
+        scale = p.grad_scale * go;
+    }
+    // pass 2: the gradient scale * exp(z - lse), from the row again
+    uint8_t* gb = static_cast<uint8_t*>(p.grad) + sp.a0;
+    const float nl = -lse * kLog2e;
+    for (int base = 0; base < sp.nvr; base += kStreamThreads * kStreamU) {
+      uint4 v[kStreamU];
+      stream_load<T, UNAL>(v, logits, sp, base, true);
+      float2 dummy = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < kStreamU; ++i) {
+        vec_exp_acc<T>(v[i], make_float2(nl, nl), dummy);
+        vec_scale<T>(v[i], scale);
+      }
+#pragma unroll
+      for (int i = 0; i < kStreamU; ++i) {
+        const int vi = base + i * kStreamThreads + static_cast<int>(threadIdx.x);
+        if (vi >= sp.nvr) continue;
+        const int lo = UNAL && vi == 0 ? sp.lead : 0, hi = UNAL && vi == sp.nvr - 1 ? sp.tail : EPV;
+        if (lo > 0 || hi < EPV)  // a vector shared with a neighbouring row: this row's elements only
+          store_elems<T>(reinterpret_cast<T*>(gb + 16ull * vi), v[i], lo, hi);
+        else
+          __stcs(reinterpret_cast<uint4*>(gb + 16ull * vi), v[i]);
+      }
+    }
+    // the target element replaces what the vector store wrote there (same thread)
+    if (own_t) static_cast<T*>(p.grad)[row * p.V + tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
+  }
+
+  if (p.loss_out != nullptr) {
+    __syncthreads();
+    ce_finish_loss(p, s_gsum - s_gcomp, nv);
+  }
+}
+
+template <typename T, bool UNAL>
+cudaError_t launch_stream_t(const CeParams& p, int grid, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  CeParams pc = p;
+  return cudaLaunchKernelEx(&cfg, ce_rows_stream_kernel<T, UNAL>, pc);
+}
+
 // Half-row ring form, for rows of 72-144 KB (fp32 logits up to V = 36864,
 // 16-bit logits up to V = 73728): each row is loaded as two halves into a
 // ring of three half-row buffers; group g of the CTA takes half g of every
@@ -1222,10 +1413,17 @@ static bool ce_half_rows_ok(int64_t V, int dtype, bool vector_path, bool aligned
   return (vector_path || aligned_ptrs) && row_bytes > 72 * 1024 && row_bytes <= 144 * 1024;
 }
 
+// Rows over 144 KB: the streaming form (16-byte-aligned pointers).
+static bool ce_stream_rows_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
+  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
+  return (vector_path || aligned_ptrs) && row_bytes > 144 * 1024 && row_bytes <= (int64_t(1) << 30);
+}
+
 bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
   const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
   return ((vector_path && row_bytes <= 144 * 1024) || ce_unaligned_ring_ok(V, dtype, vector_path, aligned_ptrs) ||
-          ce_half_rows_ok(V, dtype, vector_path, aligned_ptrs)) &&
+          ce_half_rows_ok(V, dtype, vector_path, aligned_ptrs) ||
+          ce_stream_rows_ok(V, dtype, vector_path, aligned_ptrs)) &&
          device_sm_count() <= kCeMaxFlags;
 }
 
@@ -1302,6 +1500,20 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
     if (grid > p.N) grid = static_cast<int>(p.N);
     e = vector_path ? launch_half<false>(p, dtype, vpt, half_bytes, grid, pdl, s)
                     : launch_half<true>(p, dtype, vpt, half_bytes, grid, pdl, s);
+    prof_end(s);
+    return e;
+  }
+  // longer rows: the streaming form, two CTAs per SM while the rows they hold
+  // in flight (one each) stay well inside L2, else one
+  if (ce_stream_rows_ok(p.V, dtype, vector_path, aligned_ptrs)) {
+    int grid = device_sm_count() * (row_bytes <= 256 * 1024 ? 2 : 1);
+    if (grid > p.N) grid = static_cast<int>(p.N);
+    if (dtype == FLCE_DTYPE_BF16)
+      e = vector_path ? launch_stream_t<uint16_t, false>(p, grid, pdl, s) : launch_stream_t<uint16_t, true>(p, grid, pdl, s);
+    else if (dtype == FLCE_DTYPE_FP16)
+      e = vector_path ? launch_stream_t<__half, false>(p, grid, pdl, s) : launch_stream_t<__half, true>(p, grid, pdl, s);
+    else
+      e = vector_path ? launch_stream_t<float, false>(p, grid, pdl, s) : launch_stream_t<float, true>(p, grid, pdl, s);
     prof_end(s);
     return e;
   }

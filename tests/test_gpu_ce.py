@@ -1,7 +1,7 @@
 """GPU parity of ce_fwd_bwd (cross entropy on materialised logits) against the
-fp64 oracle: bf16 and fp32 logits, in place and out of place, loss only,
-every reduction, vector and scalar row paths, register and streaming
-segments."""
+fp64 oracle: bf16, fp16 and fp32 logits, in place and out of place, loss
+only, every reduction; the row-ring, half-row, streaming (two-pass) and
+cluster forms, rows that are and are not whole 16-byte vectors."""
 import numpy as np
 import pytest
 import torch
@@ -56,7 +56,7 @@ def test_ce_config_1024x32768(dtype, reduction, in_place):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("n,v", [(37, 1000), (64, 8192), (5, 8191), (9, 100003), (3, 1), (20, 70000),
                                  (16, 262144), (33, 20004), (33, 40008), (20000, 64), (1, 32768),
-                                 (2000, 8), (16384, 72), (16385, 72)])
+                                 (2000, 8), (16384, 72), (16385, 72), (400, 75000), (330, 80001)])
 def test_ce_shapes(dtype, n, v):
     logits, t = si.make_ce_logits(n, v, 100 + n, std=2.0, dtype=dtype, ignore_frac=0.2)
     ref = O.ce_reference(logits, t, reduction="mean")
