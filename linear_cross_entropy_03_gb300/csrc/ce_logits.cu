@@ -343,7 +343,6 @@ __global__ void __launch_bounds__(kCeThreads) ce_rows_kernel(const CeParams p) {
 // pause.  Each row is copied from the ring into registers, reduced, and its
 // gradient written from the registers with 16-byte stores.
 constexpr int kRingThreads = 1024;
-constexpr int kRingWarps = kRingThreads / 32;
 constexpr int kRingMaxDepth = 4;
 constexpr int64_t kRingSmemBudget = 220 * 1024;
 
@@ -930,8 +929,8 @@ cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, b
   return cudaLaunchKernelEx(&cfg, ce_rows_ring_kernel<T, VPT, UNAL>, pc, depth);
 }
 
-// Streaming form, for rows over 144 KB (16-bit V > 73728, fp32 V > 36864),
-// too long for one SM to hold: persistent 512-thread CTAs, two per SM, take
+// Streaming form, for rows over 72 KB (16-bit V > 36864, fp32 V > 18432),
+// too long for the row ring: persistent 512-thread CTAs, two per SM, take
 // rows blockIdx.x, blockIdx.x + gridDim.x, ...; per row, pass 1 reads the row
 // from DRAM in steps of 8 vectors per thread, keeping a per-thread online
 // (max, sum of exp), and the CTA combines them into the LSE; pass 2 reads
@@ -1121,250 +1120,6 @@ cudaError_t launch_stream_t(const CeParams& p, int grid, bool pdl, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, ce_rows_stream_kernel<T, UNAL>, pc);
 }
 
-// Half-row ring form, for rows of 72-144 KB (fp32 logits up to V = 36864,
-// 16-bit logits up to V = 73728): each row is loaded as two halves into a
-// ring of three half-row buffers; group g of the CTA takes half g of every
-// row (rows blockIdx.x, blockIdx.x + gridDim.x, ...), the CTA barrier joins
-// the two halves' partials, and each group writes its half's gradient.
-// Thread 0 keeps three half-rows in flight: after row j's barrier it
-// requests the second half of row j + 1 and the first half of row j + 2.
-template <typename T, int VPT, bool UNAL>
-__global__ void __launch_bounds__(kRingThreads, 1) ce_rows_half_kernel(const CeParams p, uint32_t half_bytes) {
-  constexpr int EPV = 16 / sizeof(T);
-  extern __shared__ __align__(128) uint8_t ring_smem[];
-  __shared__ uint64_t full[3];
-  __shared__ float2 s_part[2][kRingWarps];  // per warp (max, sum of exp(z - max)), by row parity
-  __shared__ int s_abort;
-  __shared__ float s_gsum, s_gcomp;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / kGroupWarps;
-  const int gtid = threadIdx.x % kGroupThreads;
-  const uint32_t row_bytes = static_cast<uint32_t>(p.V * sizeof(T));
-  const uint32_t half_stride = (half_bytes + 127u) & ~127u;
-  const int nvec = static_cast<int>(row_bytes / 16);
-  const int hvec0 = static_cast<int>(half_bytes / 16);                 // vectors in the first half
-  // unaligned rows: the halves split the row's 16-byte-aligned covering
-  // range, whose length varies by row (group 1's half is set per row)
-  const uint64_t tail_limit = (static_cast<uint64_t>(p.N) * row_bytes) & ~15ull;
-  int hvec = grp == 0 ? hvec0 : nvec - hvec0;                           // vectors in this group's half
-  const int vbase = grp == 0 ? 0 : hvec0;                               // its first vector in the row
-  const bool full_half = !UNAL && hvec == VPT * kGroupThreads;          // no vector past the half's end
-  const int stride = gridDim.x;
-  const int n_rows = static_cast<int>(p.N);
-  const int mine = n_rows > static_cast<int>(blockIdx.x) ? (n_rows - 1 - static_cast<int>(blockIdx.x)) / stride + 1 : 0;
-  const uint32_t ring_base = smem_addr(ring_smem);
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&full[i]), 1);
-    s_abort = 0;
-    s_gsum = s_gcomp = 0.f;
-    fence_barrier_init();
-  }
-  __syncthreads();
-  const WaitCtl ctl{&s_abort, p.status, 2000000000ull};
-  // slot s = half s % 2 of the CTA's row s / 2, in buffer s % 3
-  int issued = 0;  // thread 0 only
-  auto issue_next = [&]() {
-    const int s = issued++;
-    const int j = s >> 1, h = s & 1;
-    if (j >= mine) return;
-    const int row = blockIdx.x + j * stride;
-    const uint32_t b = static_cast<uint32_t>(s % 3);
-    uint64_t src;
-    uint32_t bytes;
-    if constexpr (UNAL) {
-      const RowSpan sp = row_span<T>(row, row_bytes, tail_limit);
-      src = sp.a0 + (h ? half_bytes : 0u);
-      bytes = h == 0 ? half_bytes : static_cast<uint32_t>(sp.nld) * 16u - half_bytes;
-    } else {
-      src = static_cast<uint64_t>(row) * row_bytes + (h ? half_bytes : 0u);
-      bytes = h == 0 ? half_bytes : row_bytes - half_bytes;
-    }
-    mbar_arrive_expect_tx(smem_addr(&full[b]), bytes);
-    bulk_load(ring_base + b * half_stride, reinterpret_cast<const uint8_t*>(p.logits) + src, bytes,
-              smem_addr(&full[b]));
-  };
-  const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 3; ++i) issue_next();
-    if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
-  }
-  int nv = 1;
-  if (p.self_count) {
-    nv = cta_count_valid(p, t_first);  // while the first half-rows load
-  } else {
-    grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
-    if (p.reduction == FLCE_REDUCTION_MEAN) nv = *p.n_valid;
-  }
-
-  for (int j = 0; j < mine; ++j) {
-    const int row = blockIdx.x + j * stride;
-    const int64_t t = __ldg(p.target + row);
-    const float go = p.grad_out != nullptr ? __ldg(p.grad_out + row) : 1.f;
-    const int s = 2 * j + grp;
-    const int b = s % 3;
-    const bool ok = mbar_wait_sleep(smem_addr(&full[b]), static_cast<uint32_t>((s / 3) & 1), ctl);
-    uint4 v[VPT];
-    const uint4* sbuf = reinterpret_cast<const uint4*>(ring_smem + b * half_stride);
-    RowSpan sp = {0, 0, 0, 0, EPV};  // unaligned rows only
-    if constexpr (UNAL) {
-      sp = row_span<T>(row, row_bytes, tail_limit);
-      if (grp == 1) hvec = sp.nvr - hvec0;
-      const int loaded = grp == 0 ? hvec0 : sp.nld - hvec0;  // vectors of this half in the buffer
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int vi = i * kGroupThreads + gtid, va = vbase + vi;  // in the half, in the covering range
-        if (vi < loaded)
-          v[i] = sbuf[vi];
-        else if (vi < hvec)  // the tensor's last partial 16 bytes
-          v[i] = load_first_elems<T>(
-              reinterpret_cast<const T*>(static_cast<const uint8_t*>(p.logits) + sp.a0 + 16ull * va), sp.tail);
-        else
-          v[i] = neg_inf_vec<T>();
-        if (vi < hvec && (va == 0 || va == sp.nvr - 1))
-          mask_outside<T>(v[i], va == 0 ? sp.lead : 0, va == sp.nvr - 1 ? sp.tail : EPV);
-      }
-    } else if (full_half) {
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) v[i] = sbuf[i * kGroupThreads + gtid];
-    } else {
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int vi = i * kGroupThreads + gtid;
-        v[i] = vi < hvec ? sbuf[vi] : neg_inf_vec<T>();
-      }
-    }
-    const int64_t tcl = t - p.v_offset;
-    const bool valid = t != p.ignore_index && tcl >= 0 && tcl < p.V;
-    const int tcol = valid ? static_cast<int>(tcl) : -1;
-    const int tel = valid ? (UNAL ? sp.lead : 0) + tcol : -1;  // its element in the (covering) row
-    const int tvec = valid ? tel / EPV - vbase : -1;           // the target's vector within this half
-    const bool own_t = valid && tvec >= 0 && tvec < hvec && (tvec % kGroupThreads) == gtid;
-    // the target logit straight from this half's buffer (one shared load), or
-    // from global memory in the tensor's last partial 16 bytes
-    float zt = 0.f;
-    if (own_t) {
-      if (!UNAL || vbase + tvec < sp.nld)
-        zt = to_f<T>(reinterpret_cast<const T*>(ring_smem + b * half_stride)[tel - vbase * EPV]);
-      else
-        zt = to_f<T>(static_cast<const T*>(p.logits)[static_cast<int64_t>(row) * p.V + tcol]);
-    }
-    const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
-    const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;
-    const float2 nmL = make_float2(nm, nm);
-    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) vec_exp_acc<T>(v[i], nmL, acc);
-    const float sw = warp_sum(acc.x + acc.y);
-    if (lane == 0) s_part[j & 1][warp] = make_float2(mw, sw);
-    // one CTA barrier per row: it joins the halves' partials, frees both
-    // buffers and carries the abort vote
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0) {  // half-rows still in flight must land before leaving
-        for (int q = 2 * j; q < issued && q < 2 * mine; ++q)
-          mbar_wait_drain(smem_addr(&full[q % 3]), static_cast<uint32_t>((q / 3) & 1), 2000000000ull);
-      }
-      break;
-    }
-    if (threadIdx.x == 0) {
-      issue_next();
-      issue_next();
-    }
-    const float2 q = s_part[j & 1][lane];  // 32 warps: one partial per lane
-    const float M = warp_max(q.x);
-    const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
-    const float lse = M + logf(S);
-
-    if (p.lse_out != nullptr) {
-      if (own_t) p.zt_out[row] = zt;
-      if (threadIdx.x == 0) {
-        p.lse_out[row] = lse;
-        if (!valid) p.zt_out[row] = 0.f;
-      }
-      continue;
-    }
-    if (p.loss_out != nullptr) {  // the CTA's rows' losses, in row order (ordered by the CTA barriers)
-      if (own_t) {
-        const float y = (lse - zt) - s_gcomp;
-        const float t2 = s_gsum + y;
-        s_gcomp = (t2 - s_gsum) - y;
-        s_gsum = t2;
-      }
-    } else {
-      if (own_t) p.loss_rows[row] = lse - zt;
-      if (!valid && threadIdx.x == 0) p.loss_rows[row] = 0.f;
-    }
-    if (p.grad == nullptr) continue;
-    float scale = 0.f;
-    if (valid) {
-      if (p.reduction == FLCE_REDUCTION_MEAN)
-        scale = p.grad_scale / static_cast<float>(nv);
-      else if (p.reduction == FLCE_REDUCTION_SUM)
-        scale = p.grad_scale;
-      else
-        scale = p.grad_scale * go;
-    }
-    const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
-    T* grow = static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V;
-    if constexpr (UNAL) {
-      uint8_t* gb = static_cast<uint8_t*>(p.grad) + sp.a0;
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int vi = i * kGroupThreads + gtid, va = vbase + vi;
-        if (vi >= hvec) continue;
-        const int lo = va == 0 ? sp.lead : 0, hi = va == sp.nvr - 1 ? sp.tail : EPV;
-        if (lo > 0 || hi < EPV)  // a vector shared with a neighbouring row: this row's elements only
-          store_elems<T>(reinterpret_cast<T*>(gb + 16ull * va), v[i], lo, hi);
-        else
-          __stcs(reinterpret_cast<uint4*>(gb + 16ull * va), v[i]);
-      }
-    } else if (full_half) {
-      uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
-    } else {
-      uint4* gvec = reinterpret_cast<uint4*>(grow) + vbase + gtid;
-#pragma unroll
-      for (int i = 0; i < VPT; ++i)
-        if (i * kGroupThreads + gtid < hvec) __stcs(gvec + i * kGroupThreads, v[i]);
-    }
-    // the target element replaces what the vector store wrote there
-    if (own_t) grow[tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
-  }
-
-  if (p.loss_out != nullptr) {  // as in the row-ring form: the CTA's partial, then one CTA adds them
-    __syncthreads();
-    ce_finish_loss(p, s_gsum - s_gcomp, nv);
-  }
-}
-
-template <typename T, int VPT, bool UNAL>
-cudaError_t launch_half_t(const CeParams& p, uint32_t half_bytes, int grid, bool pdl, cudaStream_t s) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(ce_rows_half_kernel<T, VPT, UNAL>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kRingSmemBudget + 1024));
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kRingThreads);
-  cfg.dynamicSmemBytes = 3 * static_cast<size_t>((half_bytes + 127u) & ~127u);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  CeParams pc = p;
-  return cudaLaunchKernelEx(&cfg, ce_rows_half_kernel<T, VPT, UNAL>, pc, half_bytes);
-}
 
 template <typename T, int EPV>
 cudaError_t launch_ce_t(const CeParams& p, bool pdl, cudaStream_t s) {
@@ -1406,23 +1161,15 @@ static bool ce_unaligned_ring_ok(int64_t V, int dtype, bool vector_path, bool al
   return !vector_path && aligned_ptrs && row_bytes >= 32 && row_bytes <= 72 * 1024;
 }
 
-// Rows of 72-144 KB: the half-row form, for whole-vector rows and, with
-// 16-byte-aligned pointers, for the others.
-static bool ce_half_rows_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
-  const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  return (vector_path || aligned_ptrs) && row_bytes > 72 * 1024 && row_bytes <= 144 * 1024;
-}
-
-// Rows over 144 KB: the streaming form (16-byte-aligned pointers).
+// Rows over 72 KB: the streaming form (16-byte-aligned pointers).
 static bool ce_stream_rows_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
   const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  return (vector_path || aligned_ptrs) && row_bytes > 144 * 1024 && row_bytes <= (int64_t(1) << 30);
+  return (vector_path || aligned_ptrs) && row_bytes > 72 * 1024 && row_bytes <= (int64_t(1) << 30);
 }
 
 bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs) {
   const int64_t row_bytes = V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  return ((vector_path && row_bytes <= 144 * 1024) || ce_unaligned_ring_ok(V, dtype, vector_path, aligned_ptrs) ||
-          ce_half_rows_ok(V, dtype, vector_path, aligned_ptrs) ||
+  return ((vector_path && row_bytes <= 72 * 1024) || ce_unaligned_ring_ok(V, dtype, vector_path, aligned_ptrs) ||
           ce_stream_rows_ok(V, dtype, vector_path, aligned_ptrs)) &&
          device_sm_count() <= kCeMaxFlags;
 }
@@ -1435,19 +1182,6 @@ int ce_ring_depth(int64_t V, int dtype, bool vector_path, bool unaligned) {
   int64_t depth = kRingSmemBudget / ring_buffer_stride(static_cast<uint32_t>(row_bytes), unaligned);
   if (depth > kRingMaxDepth) depth = kRingMaxDepth;
   return depth >= 2 ? static_cast<int>(depth) : 0;
-}
-
-template <bool UNAL>
-static cudaError_t launch_half(const CeParams& p, int dtype, int vpt, uint32_t half_bytes, int grid, bool pdl,
-                               cudaStream_t s) {
-  if (dtype == FLCE_DTYPE_BF16)
-    return vpt <= 8 ? launch_half_t<uint16_t, 8, UNAL>(p, half_bytes, grid, pdl, s)
-                    : launch_half_t<uint16_t, 10, UNAL>(p, half_bytes, grid, pdl, s);
-  if (dtype == FLCE_DTYPE_FP16)
-    return vpt <= 8 ? launch_half_t<__half, 8, UNAL>(p, half_bytes, grid, pdl, s)
-                    : launch_half_t<__half, 10, UNAL>(p, half_bytes, grid, pdl, s);
-  return vpt <= 8 ? launch_half_t<float, 8, UNAL>(p, half_bytes, grid, pdl, s)
-                  : launch_half_t<float, 10, UNAL>(p, half_bytes, grid, pdl, s);
 }
 
 template <bool UNAL>
@@ -1489,20 +1223,7 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
     prof_end(s);
     return e;
   }
-  // rows of 72-144 KB: the half-row ring form (rows that are not whole
-  // vectors: the halves split their 16-byte-aligned covering range)
   const int64_t row_bytes = p.V * (dtype == FLCE_DTYPE_FP32 ? 4 : 2);
-  if (ce_half_rows_ok(p.V, dtype, vector_path, aligned_ptrs)) {
-    const int64_t vecs = vector_path ? row_bytes / 16 : (row_bytes + 14 + 15) / 16;
-    const uint32_t half_bytes = static_cast<uint32_t>((vecs + 1) / 2 * 16);
-    const int vpt = static_cast<int>((half_bytes / 16 + kGroupThreads - 1) / kGroupThreads);
-    int grid = device_sm_count();
-    if (grid > p.N) grid = static_cast<int>(p.N);
-    e = vector_path ? launch_half<false>(p, dtype, vpt, half_bytes, grid, pdl, s)
-                    : launch_half<true>(p, dtype, vpt, half_bytes, grid, pdl, s);
-    prof_end(s);
-    return e;
-  }
   // longer rows: the streaming form, two CTAs per SM while the rows they hold
   // in flight (one each) stay well inside L2, else one
   if (ce_stream_rows_ok(p.V, dtype, vector_path, aligned_ptrs)) {
