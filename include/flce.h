@@ -220,9 +220,9 @@ size_t ce_workspace_size(int64_t N, int64_t V, int dtype, int reduction);
  * least 32 bytes runs on 16-byte vectors (a row that is not a whole number
  * of vectors is handled through its aligned covering range, touching no
  * neighbouring row's elements); otherwise an element-by-element path runs.
- * With N <= 16384 and 16-byte aligned pointers the call is a single kernel
- * launch (no separate counting pass); otherwise a small counting kernel
- * runs first.
+ * With N <= 16384 and the vector forms the call is a single kernel launch
+ * (no separate counting pass); otherwise a small counting kernel runs
+ * first.
  */
 flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const int64_t* target,
                          int64_t N, int64_t V, int64_t ignore_index, int reduction,
