@@ -436,7 +436,8 @@ def next_rows(step, steps=5, warmup=3):
     """The widened rows on the same shapes, fewer steps: forward-only FLCE,
     FLCE with fp16 operands, with fp32 operands, FLCE on one vocabulary shard of two (forward
     partials + backward from given row statistics, every chunk), CE on fp16 /
-    fp32 logits, CE on two vocabulary shards (partials + backward)."""
+    fp32 logits, CE on bf16 logits of the FLCE vocabulary (long rows), CE on
+    two vocabulary shards (partials + backward)."""
     import torch
     flce = step.flce
     d = step.dev
@@ -533,6 +534,18 @@ def next_rows(step, steps=5, warmup=3):
                                     "frac": round(nbytes / (ms / 1e3) / 1e9 / hbm, 4), "kernel_ms": round(kms, 4),
                                     "kernel_frac": round(nbytes / (kms / 1e3) / 1e9 / hbm, 4)}
         del z
+    # CE on logits of the Llama-3 vocabulary (rows of 250 KB: the streaming form)
+    lv = v
+    zl = torch.randn(cn, lv, device=dev, dtype=torch.float32).mul_(2.0).to(torch.bfloat16)
+    tl = torch.randint(0, lv, (cn,), device=dev, dtype=torch.int64)
+    wsl = torch.empty(flce.ce_workspace_size(cn, lv, "bf16", "mean"), dtype=torch.uint8, device=dev)
+    ms, kms = time_call(flce, lambda: check(flce.ce_fwd_bwd(zl, "bf16", zl, tl, cn, lv, -100, "mean", 1.0, None, loss,
+                                                             wsl, wsl.numel(), step.status, step.stream), "ce V"),
+                        empty_l2)
+    nbytes = 2 * cn * lv * 2 + 12 * cn
+    out[f"ce_logits_bf16_{cn}x{lv}"] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                                       "frac": round(nbytes / (ms / 1e3) / 1e9 / hbm, 4)}
+    del zl, tl, wsl
     half = cv // 2
     shards = [d["logits"][:, :half].contiguous(), d["logits"][:, half:].contiguous()]
     slse = [torch.empty(cn, device=dev) for _ in shards]
