@@ -1,21 +1,25 @@
-// Cross entropy on materialised logits [N, V] (bf16 or fp32): loss and the
-// logits gradient in one pass (liger-kernel 0.0.1 -> 0.1.1 PyPI diff, README
-// "Kernels", CrossEntropy item: loss and gradient computed together, the
-// gradient optionally replacing the input; DeepSpeed PR #8540 "Changes":
-// FP32/FP16/BF16 logits).
+// Cross entropy on materialised logits [N, V] (bf16, fp16 or fp32): loss and
+// the logits gradient in one pass over the bytes (liger-kernel 0.0.1 ->
+// 0.1.1 PyPI diff, README "Kernels", CrossEntropy item: loss and gradient
+// computed together, the gradient optionally replacing the input; DeepSpeed
+// PR #8540 "Changes": FP32/FP16/BF16 logits).
 //
-// HBM-bound design: each row is split into `cluster` contiguous segments,
-// one CTA per segment, the CTAs of a row forming a thread-block cluster.  A
-// CTA holds its segment in registers (16-byte vectors, coalesced across the
-// CTA), reduces (max, sum of exp) with warp shuffles, and every warp combines
-// the row's segment partials straight from the other CTAs' shared memory
-// (distributed shared memory).  The gradient is then formed from the
-// registers and written once, so every logit is read once and written once.
-// The cluster barrier is split: the arrive that says "done reading the other
-// CTAs' partials" is issued before the gradient pass and its wait only at
-// exit.  For sum / mean the last CTA to finish adds the row losses in a fixed
-// order (deterministic) and writes the result.  Segments longer than the
-// register capacity fall back to a two-read streaming loop.
+// HBM-bound; three forms by row length, all reading every logit from DRAM
+// once and writing its gradient once:
+//  - rows up to 72 KB: the row ring -- persistent 1024-thread CTAs, one per
+//    SM, whole rows brought into a shared-memory ring by TMA bulk copies,
+//    two 512-thread groups taking alternate rows, each row held in registers
+//    from max to gradient store;
+//  - longer rows: the streaming form -- persistent 512-thread CTAs, a first
+//    pass with an online (max, sum of exp) per thread, a second pass that
+//    re-reads the row from L2 and writes the gradient;
+//  - pointers that are not 16-byte aligned: one thread-block cluster per
+//    row, each CTA a segment in registers, the row's partials combined
+//    through distributed shared memory (segments longer than the registers
+//    hold read twice).
+// Rows that are not a whole number of 16-byte vectors use the first two
+// forms through their 16-byte-aligned covering range.  For sum / mean one
+// CTA adds the per-CTA loss partials in a fixed order (deterministic).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -184,7 +184,7 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaSt
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool aligned_ptrs, bool pdl,
                            cudaStream_t s);
 // Whether rows of V elements go to a form that supports the single launch
-// (the row-ring or half-row kernel), and at most how many CTAs it launches.
+// (the row-ring or streaming kernel).
 bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 
