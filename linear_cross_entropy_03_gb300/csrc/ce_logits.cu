@@ -942,7 +942,7 @@ cudaError_t launch_ring_t(const CeParams& p, int depth, int grid, size_t smem, b
 // L2's capacity) and writes the gradient.  DRAM moves each logit once each
 // way; the exponentials are computed twice.  Rows that are not whole
 // 16-byte vectors use their 16-byte-aligned covering range, masked as in the
-// ring forms.
+// row ring.
 constexpr int kStreamThreads = 512;
 constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kStreamU = 8;  // vectors per thread per step
