@@ -33,7 +33,8 @@ def row_scales(target, reduction, ignore_index=-100, grad_scale=1.0):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-@pytest.mark.parametrize("cuts", [(0, 1000, 2200, 3000), (0, 8, 2992, 3000), (0, 1001, 3000), (0, 20004, 40008)])
+@pytest.mark.parametrize("cuts", [(0, 1000, 2200, 3000), (0, 8, 2992, 3000), (0, 1001, 3000), (0, 20004, 40008),
+                                  (0, 80001, 160000)])
 def test_ce_vocab_parallel(dtype, cuts):
     n, v = (300 if cuts[-1] <= 3000 else 64), cuts[-1]
     logits, t = si.make_ce_logits(n, v, 31, std=2.0, dtype=dtype, ignore_frac=0.1)
