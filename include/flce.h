@@ -318,8 +318,8 @@ flce_status_t ce_vp_backward(const void* logits, int dtype, void* grad_logits, c
  * CUDA runtime query with that device current); make that first call before
  * any stream capture.  All calls share the one array: calls that may overlap
  * on the GPU (unordered streams) race and must be serialised by the caller.
- * With status_dev NULL the status word is kept inside the array and cleared
- * by each call.
+ * With status_dev NULL no status is reported.  Like ce_fwd_bwd, a call with
+ * N <= 16384 and the vector forms is a single kernel launch.
  */
 flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void* grad_logits,
                                  const int64_t* target, int64_t N, int64_t V,

@@ -14,6 +14,7 @@
 // The array is found with cudaGetSymbolAddress once per device, by the first
 // call made with that device current.  Every call shares the array: calls
 // that overlap on the GPU (different streams without ordering) race on it.
+#include <atomic>
 #include <mutex>
 
 #include "flce_internal.h"
@@ -26,6 +27,8 @@ int64_t ce_vector_elems(int dtype, bool vector_path);
 namespace {
 
 constexpr size_t kHeaderBytes = 256;  // WorkspaceHeader, rounded up
+constexpr size_t kArrivalWordOffset = 192;  // the single-launch form's tagged counter, inside the header bytes
+static_assert(sizeof(flce::WorkspaceHeader) <= kArrivalWordOffset, "header overlaps the arrival word");
 constexpr size_t kScratchBytes = kHeaderBytes + sizeof(float) * FLCE_NOALLOC_MAX_ROWS;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -82,14 +85,40 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
   float* loss_rows =
       reduction == FLCE_REDUCTION_NONE ? loss : reinterpret_cast<float*>(scratch + kHeaderBytes);
 
+  const bool ptrs16 = aligned_to(logits, 16) && (grad_logits == nullptr || aligned_to(grad_logits, 16));
+  const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && ptrs16;
+  if (N > 0 && N <= kCeSelfCountMaxRows && ce_rows_single_launch_ok(V, dtype, vec, ptrs16)) {
+    // one launch: the row kernel counts the targets itself and finds the CTA
+    // that adds the loss partials by a nonce-tagged counter in the scratch
+    // header, so nothing needs zeroing first
+    static std::atomic<unsigned long long> nonce{0x7F4A7C159E3779B9ull};
+    CeParams p = {};
+    p.logits = logits;
+    p.grad = grad_logits;
+    p.target = target;
+    p.N = N;
+    p.V = V;
+    p.ignore_index = ignore_index;
+    p.reduction = reduction;
+    p.grad_scale = grad_scale;
+    p.grad_out = grad_out_none;
+    p.loss_rows = loss_rows;
+    p.status = status_dev;
+    p.cluster = 1;
+    p.seg_len = V;
+    p.loss_out = reduction != FLCE_REDUCTION_NONE ? loss : nullptr;
+    p.self_count = 1;
+    p.done_flags = reinterpret_cast<unsigned long long*>(scratch + kArrivalWordOffset);
+    p.nonce = (nonce.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
+    return launch_ce_rows(p, dtype, vec, ptrs16, false, stream) == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
+  }
+
   // The header (valid-target count, block ticket, status) must start at zero.
   if (cudaMemsetAsync(hdr, 0, kHeaderBytes, stream) != cudaSuccess) return FLCE_ERR_CUDA;
   if (launch_count_targets(target, N, V, ignore_index, hdr, 0, 0, status, nullptr, nullptr, 0, nullptr, stream) !=
       cudaSuccess)
     return FLCE_ERR_CUDA;
   if (N > 0) {
-    const bool ptrs16 = aligned_to(logits, 16) && (grad_logits == nullptr || aligned_to(grad_logits, 16));
-    const bool vec = (static_cast<size_t>(V) * esz) % 16 == 0 && ptrs16;
     const int64_t cap = ce_cta_capacity(dtype, vec);
     const int64_t epv = ce_vector_elems(dtype, vec);
     int64_t cl = ceil_div64(V, cap);

@@ -36,7 +36,9 @@ def _without_workspace(z, t, n, v, reduction):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
-    cases = [(si.make_ce_logits(1024, 32768, 1002), "mean"), (si.make_ce_logits(300, 5000, 7), "sum")]
+    # one launch for N <= 16384; the counting kernel + ticket form beyond
+    cases = [(si.make_ce_logits(1024, 32768, 1002), "mean"), (si.make_ce_logits(300, 5000, 7), "sum"),
+             (si.make_ce_logits(20000, 64, 9), "mean"), (si.make_ce_logits(513, 5003, 11), "mean")]
     for (logits, tgt), reduction in cases:
         n, v = logits.shape
         z = dev_bf16(logits)
