@@ -577,6 +577,17 @@ __device__ __forceinline__ bool group_sync_or(uint32_t id, uint32_t count, bool 
 // loaded by the caller before it requested the first rows, so that load is
 // ahead of them in the memory queue.  All threads of the CTA must call it.
 __device__ int cta_count_valid(const CeParams& p, int64_t t_first) {
+  if (p.N <= blockDim.x) {  // one target per thread at most: one counting barrier
+    bool valid = false, bad = false;
+    if (threadIdx.x < p.N && t_first != p.ignore_index) {
+      valid = t_first >= 0 && t_first < p.V;
+      bad = !valid;
+    }
+    const int total = __syncthreads_count(valid);
+    if (__syncthreads_or(bad) && blockIdx.x == 0 && threadIdx.x == 0 && p.status != nullptr)
+      atomicOr(p.status, FLCE_STATUS_BIT_TARGET_RANGE);
+    return total;
+  }
   __shared__ int s_count;
   if (threadIdx.x == 0) s_count = 0;
   __syncthreads();
@@ -801,12 +812,17 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     // the target logit straight from the ring buffer (one shared load; the
     // buffer is not refilled before this group's barrier), or from global
     // memory in the tensor's last partial 16 bytes
-    float zt = 0.f;
-    if (own_t) {
-      if (!UNAL || tvec < sp.nld)
-        zt = to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tel]);
-      else
-        zt = to_f<T>(static_cast<const T*>(p.logits)[static_cast<int64_t>(row) * p.V + tcol]);
+    float zt;
+    if constexpr (UNAL) {
+      zt = 0.f;
+      if (own_t) {
+        if (tvec < sp.nld)
+          zt = to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tel]);
+        else
+          zt = to_f<T>(static_cast<const T*>(p.logits)[static_cast<int64_t>(row) * p.V + tcol]);
+      }
+    } else {
+      zt = own_t ? to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tcol]) : 0.f;
     }
     // warp max, then exp(z - warp max) in place and its warp sum
     const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
