@@ -440,7 +440,10 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
     p.grad_scale = grad_scale;
     p.grad_out = grad_out_none;
     p.loss_rows = loss_rows;
-    p.status = status_dev;
+    // the status word: the caller's, or the workspace's own, which CTA 0
+    // clears when it starts (the other CTAs only write it after a 2 s wait)
+    p.status = status;
+    p.clear_status = status_dev == nullptr ? 1 : 0;
     p.cluster = 1;
     p.seg_len = V;
     p.loss_out = reduction != FLCE_REDUCTION_NONE ? loss : nullptr;

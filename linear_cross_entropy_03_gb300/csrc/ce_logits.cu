@@ -749,6 +749,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   if (threadIdx.x == 0) {
     for (int i = 0; i < first && i < mine; ++i) issue(i, blockIdx.x + i * stride);
     if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+    if (blockIdx.x == 0 && p.clear_status) *p.status = 0;  // before this CTA flags anything
   }
   const bool full_rows = !UNAL && nvec == VPT * kGroupThreads;  // no vector past the row's end
   int nv = 1;
@@ -995,6 +996,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) ce_rows_stream_kernel(const
   if (threadIdx.x == 0) {
     s_gsum = s_gcomp = 0.f;
     if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+    if (blockIdx.x == 0 && p.clear_status) *p.status = 0;  // before this CTA flags anything
   }
   int nv = 1;
   if (p.self_count) {

@@ -121,6 +121,7 @@ struct CeParams {
   int self_count;
   unsigned long long* done_flags;  // the tagged counter (one word), or null: use `ticket`
   unsigned long long nonce;        // below 2^40, different from the previous call's
+  int clear_status;                // CTA 0 zeroes *status when it starts (the workspace's own word)
 };
 
 // Most rows the single-launch CE form takes (each CTA reads every target).

@@ -158,3 +158,22 @@ def test_ce_without_status_word():
     assert st == 0
     assert_loss(host(loss)[0], ref["loss"], "mean")
     assert_grad(host(z), ref["dz"], "grad_logits")
+
+
+def test_ce_status_in_workspace_when_no_status_word():
+    # status_dev NULL: the status lives in the workspace's first 4 bytes and
+    # each call starts it from zero (the single-launch form clears it in CTA 0)
+    n, v = 50, 300
+    ws = torch.full((flce.ce_workspace_size(n, v, "bf16", "mean"),), 0x7F, dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    for bad in (True, False):
+        logits, t = si.make_ce_logits(n, v, 6)
+        if bad:
+            t[4] = v
+        z = dev_bf16(logits)
+        st = flce.ce_fwd_bwd(z, "bf16", z, torch.from_numpy(t).cuda(), n, v, -100, "mean", 1.0, None, loss, ws,
+                             ws.numel(), None, None)
+        torch.cuda.synchronize()
+        assert st == 0
+        word = int(ws[:4].view(torch.int32).item())
+        assert word == (0x1 if bad else 0), hex(word)
