@@ -67,7 +67,14 @@ typedef enum {
   FLCE_REDUCTION_MEAN = 2  /* sum / number of valid rows (NaN if 0)   */
 } flce_reduction_t;
 
-typedef enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1, FLCE_DTYPE_FP16 = 2 } flce_dtype_t;
+/* FLCE_DTYPE_FP32_ROUNDED: fp32 FLCE operands rounded to bf16 once (the
+ * fast mode of flce_fwd_bwd_typed); not a logits type. */
+typedef enum {
+  FLCE_DTYPE_BF16 = 0,
+  FLCE_DTYPE_FP32 = 1,
+  FLCE_DTYPE_FP16 = 2,
+  FLCE_DTYPE_FP32_ROUNDED = 3
+} flce_dtype_t;
 
 typedef enum {
   FLCE_OK = 0,
@@ -157,15 +164,18 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
 
 /*
  * flce_fwd_bwd_typed -- flce_fwd_bwd with the operand type given: dtype is
- *   FLCE_DTYPE_BF16  exactly flce_fwd_bwd;
- *   FLCE_DTYPE_FP16  hidden, weight, bias and grad_hidden are IEEE half;
- *   FLCE_DTYPE_FP32  hidden, weight, bias and grad_hidden are fp32;
+ *   FLCE_DTYPE_BF16          exactly flce_fwd_bwd;
+ *   FLCE_DTYPE_FP16          hidden, weight, bias and grad_hidden are IEEE half;
+ *   FLCE_DTYPE_FP32          hidden, weight, bias and grad_hidden are fp32,
+ *                            multiplied at about fp32 accuracy (below);
+ *   FLCE_DTYPE_FP32_ROUNDED  the same buffers, the operands rounded to bf16
+ *                            once (the fast mode, below);
  * everything else is as in flce_fwd_bwd.  The workspace must hold
  * flce_workspace_size_typed(dtype, ...) bytes (the same as
- * flce_workspace_size for the two 16-bit types; fp32 adds room for the bf16
- * copies of hidden, weight and bias).  Other dtypes return
- * FLCE_ERR_UNSUPPORTED, and so does fp16 / fp32 while the one-CTA GEMM form
- * is selected (flce_set_gemm_variant).  The logits dtypes FP32 / FP16 / BF16
+ * flce_workspace_size for the two 16-bit types; FP32 adds bf16 hi + lo
+ * copies of hidden and weight and a second plane of chunk logits,
+ * FP32_ROUNDED one bf16 copy of hidden, weight and bias).  Other dtypes return
+ * FLCE_ERR_UNSUPPORTED.  The logits dtypes FP32 / FP16 / BF16
  * the DeepSpeed PR #8540 description ("optional Liger vocab-parallel CE
  * backend", section "Changes") validates carry over to the fused form here.
  *
@@ -177,13 +187,22 @@ flce_status_t flce_fwd_bwd(const void* hidden, const void* weight, const void* b
  * two backward products multiply that factor back in fp32.  grad_bias is
  * summed from the fp32 grad-logits.
  *
- * Arithmetic with fp32: hidden, weight and bias are rounded to bf16 (to
- * nearest, ties to even) into the workspace once per call and the bf16 path
- * runs on those copies, so the loss and grad_weight / grad_bias equal the
- * bf16 entry point's on the rounded inputs; grad_hidden is written from the
- * fp32 accumulator without the bf16 rounding.  (The mixed-precision recipe
- * the fused kernel serves computes in 16-bit; fp32 operands are accepted for
- * callers whose master copies are fp32.)
+ * Arithmetic with FP32: hidden and weight are split once per call into bf16
+ * hi = round(x) and lo = round(x - hi) (nearest, ties to even), and every
+ * product is formed on the tensor cores as hi.hi + hi.lo + lo.hi with fp32
+ * accumulation (the dropped lo.lo term is below 2^-16 of each product), at
+ * a third of the bf16 tensor rate; the bias is added in fp32; the chunk
+ * logits are kept exactly (both halves of their fp32 bits), their gradient
+ * is formed in fp32 and split the same way for the two backward products;
+ * grad_hidden is written from the fp32 accumulator.
+ *
+ * Arithmetic with FP32_ROUNDED: hidden, weight and bias are rounded to bf16
+ * (to nearest, ties to even) into the workspace once per call and the bf16
+ * path runs on those copies, so the loss and grad_weight / grad_bias equal
+ * the bf16 entry point's on the rounded inputs; grad_hidden is written from
+ * the fp32 accumulator without the bf16 rounding.  This is the rate of the
+ * bf16 path at its precision, for callers whose fp32 tensors are master
+ * copies of a mixed-precision step.
  */
 flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weight, const void* bias,
                                  const int64_t* target, int64_t N, int64_t H, int64_t V,
@@ -311,11 +330,17 @@ flce_status_t ce_vp_backward(const void* logits, int dtype, void* grad_logits, c
  * the library, sized for FLCE_NOALLOC_MAX_ROWS rows (about 256 KiB, held by
  * every GPU that loads the library until the process exits).  Arguments are
  * those of ce_fwd_bwd without the workspace; N > FLCE_NOALLOC_MAX_ROWS returns
- * FLCE_ERR_UNSUPPORTED before anything is enqueued.  Nothing is allocated or
- * freed, by the library or by any routine it calls.
+ * FLCE_ERR_UNSUPPORTED before anything is enqueued.  The entry point calls
+ * no allocating routine (no cudaMalloc or cudaFree, no workspace).  Device
+ * memory does appear once per device context when the CUDA runtime loads the
+ * library's module (the array and the kernels' code; with lazy module
+ * loading, the default, this happens at the first call and at the first
+ * launch of each kernel): make one warm-up call per device outside any
+ * region that must not allocate.
  *
- * The first call on a device looks the array's device address up (a one-time
- * CUDA runtime query with that device current); make that first call before
+ * The first call on a device context looks the array's device address up (a
+ * CUDA runtime query with that device current; again after cudaDeviceReset,
+ * whose new context holds the array elsewhere); make that first call before
  * any stream capture.  All calls share the one array: calls that may overlap
  * on the GPU (unordered streams) race and must be serialised by the caller.
  * With status_dev NULL no status is reported.  Like ce_fwd_bwd, a call with
@@ -330,14 +355,6 @@ flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void* grad_logit
 /* ------------------------------------------------------------------------
  * Diagnostics (no counterpart on the pages)
  * ------------------------------------------------------------------------ */
-
-/* Tensor-core kernel form used by flce_fwd_bwd calls enqueued afterwards:
- * FLCE_GEMM_CTA_PAIR (the default: 256 x 256 tiles on a pair of SMs, tcgen05
- * cta_group::2) or FLCE_GEMM_SINGLE_CTA (128 x 256 tiles, one CTA per tile).
- * 0 selects the default.  Returns the form now in effect. */
-#define FLCE_GEMM_SINGLE_CTA 1
-#define FLCE_GEMM_CTA_PAIR 2
-int flce_set_gemm_variant(int variant);
 
 /* Time limit of every pipeline wait inside the kernels, in nanoseconds of
  * %globaltimer (default 2e9).  Applies to calls enqueued afterwards. */
@@ -362,7 +379,8 @@ enum {
   FLCE_KERNEL_GEMM_BWD = 4,
   FLCE_KERNEL_LOSS_REDUCE = 5,
   FLCE_KERNEL_CE_ROWS = 6,
-  FLCE_KERNEL_ZERO = 7
+  FLCE_KERNEL_ZERO = 7,
+  FLCE_KERNEL_BIAS_REDUCE = 8
 };
 const char* flce_kernel_name(int kernel_id);
 flce_status_t flce_profile_enable(int capacity);

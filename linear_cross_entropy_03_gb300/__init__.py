@@ -19,17 +19,17 @@ __all__ = [
     "library_path", "lib", "flce_status_string", "flce_version", "flce_default_chunk",
     "flce_workspace_size", "flce_workspace_size_typed", "flce_fwd_bwd", "flce_fwd_bwd_typed", "ce_workspace_size", "ce_fwd_bwd", "ce_fwd_bwd_noalloc",
     "flce_vp_workspace_size", "flce_vp_forward", "flce_vp_backward", "ce_vp_partials", "ce_vp_backward",
-    "flce_set_gemm_variant", "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
+    "flce_set_wait_timeout_ns", "flce_selftest_wait_timeout", "flce_kernel_name",
     "flce_profile_enable", "flce_profile_disable", "flce_profile_read",
     "fused_linear_cross_entropy", "cross_entropy", "FlceError",
 ]
 
 REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
-DTYPES = {"bf16": 0, "fp32": 1, "fp16": 2}
+DTYPES = {"bf16": 0, "fp32": 1, "fp16": 2, "fp32_rounded": 3}
 STATUS_BIT_TARGET_RANGE = 0x1
 STATUS_BIT_TIMEOUT = 0x2
 KERNEL_NAMES = ("count_targets", "gemm_forward", "row_finalize", "grad_logits", "gemm_backward",
-                "loss_reduce", "ce_rows", "zero")
+                "loss_reduce", "ce_rows", "zero", "bias_reduce")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libflce03.so")
@@ -55,7 +55,6 @@ _SIGNATURES = {
                                   ctypes.c_float, _P, _P, _P, _SZ, _P, _P]),
     "ce_fwd_bwd_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                           ctypes.c_float, _P, _P, _P, _P]),
-    "flce_set_gemm_variant": (ctypes.c_int, [ctypes.c_int]),
     "flce_vp_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "flce_vp_forward": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ,
                                        _P, _P]),
@@ -229,16 +228,6 @@ def ce_vp_backward(logits, dtype, grad_logits, target, N, V_shard, vocab_offset,
                                 _stream(stream))
 
 
-GEMM_SINGLE_CTA = 1
-GEMM_CTA_PAIR = 2
-
-
-def flce_set_gemm_variant(variant: int) -> int:
-    """Select the tensor-core kernel form (1: one CTA per 128x256 tile,
-    2: CTA pairs on 256x256 tiles, 0: default); returns the form in effect."""
-    return lib().flce_set_gemm_variant(int(variant))
-
-
 def flce_set_wait_timeout_ns(ns: int) -> None:
     lib().flce_set_wait_timeout_ns(int(ns))
 
@@ -278,7 +267,8 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
                                reduction="mean", chunk: int = 0, grad_scale: float = 1.0,
                                grad_out=None, grad_hidden: bool = True, grad_weight: bool = True,
                                grad_weight_out=None, grad_bias_out=None, accumulate: bool = False,
-                               row_stats: bool = False, workspace=None, status=None, stream=None) -> dict:
+                               row_stats: bool = False, fp32_mode: str = "split", workspace=None, status=None,
+                               stream=None) -> dict:
     """Loss and gradients of cross_entropy(hidden @ weight.T + bias, target).
 
     hidden [N, H] and weight [V, H] bf16, fp16 or fp32 (both the same), bias
@@ -286,9 +276,11 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
     contiguous.  Returns a dict with ``loss`` (fp32 [N] or []),
     ``grad_hidden`` ([N, H], the input type), ``grad_weight``
     (fp32 [V, H]), ``grad_bias`` (fp32 [V]), ``n_valid`` (int32 [1]) and, with
-    ``row_stats``, ``lse`` and ``target_logit`` (fp32 [N]).  Asynchronous on
-    ``stream`` (default: the current stream); ``status`` is the device
-    status word (int32 [1]).
+    ``row_stats``, ``lse`` and ``target_logit`` (fp32 [N]).  fp32 operands
+    run split into bf16 hi + lo (``fp32_mode="split"``, three products) or
+    rounded to bf16 once (``"rounded"``).  Asynchronous on ``stream``
+    (default: the current stream); ``status`` is the device status word
+    (int32 [1]).
     """
     import torch
     n, h = hidden.shape
@@ -299,6 +291,10 @@ def fused_linear_cross_entropy(hidden, weight, target, bias=None, *, ignore_inde
     dtype = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}.get(hidden.dtype)
     if dtype is None or weight.dtype != hidden.dtype or (bias is not None and bias.dtype != hidden.dtype):
         raise FlceError(2, "fused_linear_cross_entropy: hidden, weight and bias must share one of bf16/fp16/fp32")
+    if dtype == "fp32" and fp32_mode == "rounded":
+        dtype = "fp32_rounded"
+    elif dtype == "fp32" and fp32_mode != "split":
+        raise FlceError(1, f"fused_linear_cross_entropy: fp32_mode {fp32_mode!r}")
     gh = torch.empty(n, h, dtype=hidden.dtype, device=dev) if grad_hidden else None
     gw = grad_weight_out if grad_weight_out is not None else (
         torch.empty(v, h, dtype=torch.float32, device=dev) if grad_weight else None)

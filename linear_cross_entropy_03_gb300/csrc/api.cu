@@ -28,7 +28,6 @@ constexpr size_t kAlign = 256;
 constexpr int64_t kDefaultChunkBudget = int64_t(2) << 30;
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
-std::atomic<int> g_gemm_variant{FLCE_GEMM_CTA_PAIR};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -80,6 +79,7 @@ struct FlceLayout {
   int64_t chunk, num_chunks, vp, nvt;
   size_t header, zbuf, partials, tgt_logit, row_lse, row_scale, row_tgt, loss_rows, total;
   size_t cvt_h, cvt_w, cvt_b;  // fp32 operands: their bf16 copies (0 bytes otherwise)
+  int64_t z_plane;             // split fp32 operands: elements between the two chunk-logit planes (else 0)
 };
 
 int64_t default_chunk(int64_t N, int64_t V) {
@@ -104,10 +104,21 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   size_t off = 0;
   L->header = off;
   off = round_up(off + sizeof(WorkspaceHeader) + sizeof(unsigned int) * 2 * (L->num_chunks + 1), kAlign);
+  // split fp32 operands (FLCE_DTYPE_FP32): the chunk logits as two planes of
+  // 16-bit halves, and hi + lo bf16 planes of hidden and weight; the bias is
+  // read in fp32.  Rounded fp32 operands: one bf16 copy of each.
+  const bool split = dtype == FLCE_DTYPE_FP32;
+  const bool rounded = dtype == FLCE_DTYPE_FP32_ROUNDED;
+  const size_t planes = split ? 2 : 1;
   L->zbuf = off;
-  off = round_up(off + static_cast<size_t>(L->chunk) * L->vp * 2, kAlign);
+  L->z_plane = split ? L->chunk * static_cast<int64_t>(L->vp) : 0;
+  off = round_up(off + planes * static_cast<size_t>(L->chunk) * L->vp * 2, kAlign);
   L->partials = off;
-  off = round_up(off + static_cast<size_t>(L->chunk) * L->nvt * sizeof(float4), kAlign);
+  // the per-tile partials of the forward epilogue; after row_finalize the same
+  // bytes take the grad-logits pass's per-row-block bias column sums
+  off = round_up(off + std::max(static_cast<size_t>(L->chunk) * L->nvt * sizeof(float4),
+                                static_cast<size_t>(ceil_div(L->chunk, kGlBiasRows)) * L->vp * sizeof(float)),
+                 kAlign);
   L->tgt_logit = off;
   off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
   L->row_lse = off;
@@ -118,13 +129,13 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
   L->loss_rows = off;
   off = round_up(off + (reduction == FLCE_REDUCTION_NONE ? 0 : static_cast<size_t>(N) * 4), kAlign);
-  const bool f32 = dtype == FLCE_DTYPE_FP32;
+  const size_t copies = split ? 2 : (rounded ? 1 : 0);
   L->cvt_h = off;
-  off = round_up(off + (f32 ? static_cast<size_t>(N) * H * 2 : 0), kAlign);
+  off = round_up(off + copies * static_cast<size_t>(N) * H * 2, kAlign);
   L->cvt_w = off;
-  off = round_up(off + (f32 ? static_cast<size_t>(V) * H * 2 : 0), kAlign);
+  off = round_up(off + copies * static_cast<size_t>(V) * H * 2, kAlign);
   L->cvt_b = off;
-  off = round_up(off + (f32 ? static_cast<size_t>(L->vp) * 2 : 0), kAlign);
+  off = round_up(off + (rounded ? static_cast<size_t>(L->vp) * 2 : 0), kAlign);
   L->total = off;
   return true;
 }
@@ -140,7 +151,7 @@ bool ce_layout(int64_t N, int64_t V, int dtype, int reduction, CeLayout* L) {
   L->header = 0;
   L->loss_rows = round_up(sizeof(WorkspaceHeader) + 16, kAlign);
   L->flags = round_up(L->loss_rows + static_cast<size_t>(N) * 4, kAlign);
-  L->total = round_up(L->flags + sizeof(unsigned long long), kAlign);
+  L->total = round_up(L->flags + sizeof(unsigned long long), kAlign);  // the tagged arrival counter
   return true;
 }
 
@@ -210,7 +221,9 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk, int r
 }
 
 size_t flce_workspace_size_typed(int dtype, int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction) {
-  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16 && dtype != FLCE_DTYPE_FP32) return 0;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16 && dtype != FLCE_DTYPE_FP32 &&
+      dtype != FLCE_DTYPE_FP32_ROUNDED)
+    return 0;
   FlceLayout L;
   if (!flce_layout(N, H, V, chunk, reduction, &L, dtype)) return 0;
   return L.total;
@@ -237,11 +250,13 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FlceLayout L;
   if (N < 0 || V < 1 || H < 1 || chunk < 0 || reduction < 0 || reduction > 2) return FLCE_ERR_INVALID_ARG;
-  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16 && dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
-  const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_FP16 && dtype != FLCE_DTYPE_FP32 &&
+      dtype != FLCE_DTYPE_FP32_ROUNDED)
+    return FLCE_ERR_UNSUPPORTED;
   const bool fp16 = dtype == FLCE_DTYPE_FP16;
-  const bool fp32 = dtype == FLCE_DTYPE_FP32;
-  if ((fp16 || fp32) && !pair) return FLCE_ERR_UNSUPPORTED;  // fp16 / fp32 operands: the CTA-pair kernels only
+  const bool split = dtype == FLCE_DTYPE_FP32;            // hi + lo bf16 planes, three products
+  const bool rounded = dtype == FLCE_DTYPE_FP32_ROUNDED;  // one bf16 rounding
+  const bool fp32 = split || rounded;
   if (H % 8 != 0) return FLCE_ERR_UNSUPPORTED;
   if (!flce_layout(N, H, V, chunk, reduction, &L, dtype)) return FLCE_ERR_INVALID_ARG;
   if (loss == nullptr || weight == nullptr) return FLCE_ERR_INVALID_ARG;
@@ -278,7 +293,20 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     return FLCE_OK;
   }
 
-  if (fp32) {
+  CUtensorMap tm_h2, tm_w2, tm_z2;  // split: the lo planes
+  if (split) {
+    // fp32 operands split into bf16 hi + lo planes once per call; the
+    // products are hi.hi + hi.lo + lo.hi (grad_hidden written in fp32)
+    uint16_t* h_hi = reinterpret_cast<uint16_t*>(ws + L.cvt_h);
+    uint16_t* h_lo = h_hi + N * H;
+    uint16_t* w_hi = reinterpret_cast<uint16_t*>(ws + L.cvt_w);
+    uint16_t* w_lo = w_hi + V * H;
+    FLCE_TRY_CUDA(launch_f32_split_bf16(static_cast<const float*>(hidden), h_hi, h_lo, N * H, stream));
+    FLCE_TRY_CUDA(launch_f32_split_bf16(static_cast<const float*>(weight), w_hi, w_lo, V * H, stream));
+    if (!make_map(&tm_h2, h_lo, H, N, H) || !make_map(&tm_w2, w_lo, H, V, H)) return FLCE_ERR_CUDA;
+    hidden = h_hi;
+    weight = w_hi;
+  } else if (rounded) {
     // fp32 operands: the tensor cores take their bf16 roundings, copied once
     // per call into the workspace (grad_hidden is still written in fp32)
     uint16_t* h16 = reinterpret_cast<uint16_t*>(ws + L.cvt_h);
@@ -305,6 +333,7 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     const int64_t row0 = k * L.chunk;
     const int c_len = static_cast<int>(std::min<int64_t>(L.chunk, N - row0));
     if (!make_map(&tm_z, zbuf, V, c_len, L.vp, mtype)) return FLCE_ERR_CUDA;
+    if (split && !make_map(&tm_z2, zbuf + L.z_plane, V, c_len, L.vp)) return FLCE_ERR_CUDA;
 
     GemmParams g = {};
     g.row0 = row0;
@@ -313,7 +342,10 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     g.V = static_cast<int>(V);
     g.f_num_m = static_cast<int>(ceil_div(c_len, kBM));
     g.f_kblocks = static_cast<int>(ceil_div(H, kBK));
-    g.bias = static_cast<const uint16_t*>(bias);
+    g.bias = split ? nullptr : static_cast<const uint16_t*>(bias);
+    g.bias_f32 = split ? static_cast<const float*>(bias) : nullptr;
+    g.nseg = split ? 3 : 1;
+    g.z_plane = L.z_plane;
     g.target = target;
     g.zbuf = zbuf;
     g.ldz = L.vp;
@@ -332,14 +364,12 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     g.reduction = reduction;
     g.grad_scale = grad_scale;
 
-    const int tile_m = pair ? 2 * kBM : kBM;
+    const int tile_m = 2 * kBM;  // CTA-pair tiles: 256 rows
     g.f_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.num_tiles = static_cast<int>(g.f_num_m * L.nvt);
     g.tile_counter = &hdr->tile_counters[2 * k];
-    if (pair)
-      FLCE_TRY_CUDA(launch_gemm2(kModeForward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
-    else
-      FLCE_TRY_CUDA(launch_gemm(kModeForward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+    FLCE_TRY_CUDA(launch_gemm2(kModeForward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream,
+                               split ? &tm_h2 : nullptr, split ? &tm_w2 : nullptr, split ? &tm_z2 : nullptr));
 
     RowParams r = {};
     r.row0 = row0;
@@ -365,7 +395,9 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     r.zbuf = zbuf;
     r.ldz = L.vp;
     r.grad_bias = grad_bias;
+    r.bias_part = reinterpret_cast<float*>(ws + L.partials);
     r.z_fp16 = fp16 ? 1 : 0;
+    r.z_plane = L.z_plane;
     r.gmax = gmax;
     FLCE_TRY_CUDA(launch_row_finalize(r, stream));
     if (!want_grads) continue;
@@ -373,19 +405,16 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
 
     g.h_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.h_kblocks = static_cast<int>(ceil_div(V, kBK));
-    // the pair form computes grad_H in 256 x 512 tiles, the one-CTA form in 128 x 256
-    g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, pair ? 2 * kBN : kBN)) : 0;
+    // grad_H in 256 x 512 tiles
+    g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, 2 * kBN)) : 0;
     g.w_num_n = static_cast<int>(ceil_div(H, kBN));
     g.w_kblocks = static_cast<int>(ceil_div(c_len, kBK));
     const int w_tiles = grad_weight != nullptr ? static_cast<int>(ceil_div(V, tile_m) * g.w_num_n) : 0;
     g.num_tiles = g.h_tiles + w_tiles;
     g.tile_counter = &hdr->tile_counters[2 * k + 1];
-    if (g.num_tiles > 0) {
-      if (pair)
-        FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
-      else
-        FLCE_TRY_CUDA(launch_gemm(kModeBackward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
-    }
+    if (g.num_tiles > 0)
+      FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream,
+                                 split ? &tm_h2 : nullptr, split ? &tm_w2 : nullptr, split ? &tm_z2 : nullptr));
   }
   if (reduction != FLCE_REDUCTION_NONE)
     FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, false));
@@ -493,13 +522,6 @@ flce_status_t ce_fwd_bwd(const void* logits, int dtype, void* grad_logits, const
   return FLCE_OK;
 }
 
-int flce_set_gemm_variant(int variant) {
-  if (variant == 0) variant = FLCE_GEMM_CTA_PAIR;
-  if (variant != FLCE_GEMM_SINGLE_CTA && variant != FLCE_GEMM_CTA_PAIR) return g_gemm_variant.load();
-  g_gemm_variant.store(variant);
-  return variant;
-}
-
 // ------------------------------------------------------------ vocabulary shards
 
 size_t flce_vp_workspace_size(int64_t C, int64_t H, int64_t V_shard) {
@@ -533,8 +555,7 @@ flce_status_t flce_vp_forward(const void* hidden, const void* weight_shard, cons
   if (!make_map(&tm_h, hidden, H, C, H) || !make_map(&tm_w, weight_shard, H, V_shard, H) ||
       !make_map(&tm_z, ws + L.zbuf, V_shard, C, L.vp))
     return FLCE_ERR_CUDA;
-  const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
-  const int tile_m = pair ? 2 * kBM : kBM;
+  const int tile_m = 2 * kBM;
   GemmParams g = {};
   g.row0 = 0;
   g.c_len = static_cast<int>(C);
@@ -555,10 +576,7 @@ flce_status_t flce_vp_forward(const void* hidden, const void* weight_shard, cons
   g.num_tiles = static_cast<int>(g.f_num_m * L.nvt);
   g.tile_counter = &hdr->tile_counters[0];
   const int sms = device_sm_count();
-  if (pair)
-    FLCE_TRY_CUDA(launch_gemm2(kModeForward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
-  else
-    FLCE_TRY_CUDA(launch_gemm(kModeForward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+  FLCE_TRY_CUDA(launch_gemm2(kModeForward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
   RowParams r = {};
   r.row0 = 0;
   r.c_len = static_cast<int>(C);
@@ -612,14 +630,14 @@ flce_status_t flce_vp_backward(const void* hidden, const void* weight_shard, con
   r.zbuf = reinterpret_cast<uint16_t*>(ws + L.zbuf);
   r.ldz = L.vp;
   r.grad_bias = grad_bias_shard;
+  r.bias_part = reinterpret_cast<float*>(ws + L.partials);
   FLCE_TRY_CUDA(launch_grad_logits(r, stream));
   if (grad_hidden_partial == nullptr && grad_weight_shard == nullptr) return FLCE_OK;
   CUtensorMap tm_h, tm_w, tm_z;
   if (!make_map(&tm_h, hidden, H, C, H) || !make_map(&tm_w, weight_shard, H, V_shard, H) ||
       !make_map(&tm_z, ws + L.zbuf, V_shard, C, L.vp))
     return FLCE_ERR_CUDA;
-  const bool pair = g_gemm_variant.load() == FLCE_GEMM_CTA_PAIR;
-  const int tile_m = pair ? 2 * kBM : kBM;
+  const int tile_m = 2 * kBM;
   GemmParams g = {};
   g.row0 = 0;
   g.c_len = static_cast<int>(C);
@@ -637,17 +655,14 @@ flce_status_t flce_vp_backward(const void* hidden, const void* weight_shard, con
   g.h_num_m = static_cast<int>(ceil_div(C, tile_m));
   g.h_kblocks = static_cast<int>(ceil_div(V_shard, kBK));
   g.h_tiles =
-      grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, pair ? 2 * kBN : kBN)) : 0;
+      grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, 2 * kBN)) : 0;
   g.w_num_n = static_cast<int>(ceil_div(H, kBN));
   g.w_kblocks = static_cast<int>(ceil_div(C, kBK));
   const int w_tiles = grad_weight_shard != nullptr ? static_cast<int>(ceil_div(V_shard, tile_m) * g.w_num_n) : 0;
   g.num_tiles = g.h_tiles + w_tiles;
   g.tile_counter = &hdr->tile_counters[1];
   const int sms = device_sm_count();
-  if (pair)
-    FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
-  else
-    FLCE_TRY_CUDA(launch_gemm(kModeBackward, tm_h, tm_w, tm_z, g, std::min(sms, g.num_tiles), stream));
+  FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
   return FLCE_OK;
 }
 
@@ -735,6 +750,7 @@ const char* flce_kernel_name(int id) {
     case FLCE_KERNEL_LOSS_REDUCE: return "loss_reduce";
     case FLCE_KERNEL_CE_ROWS: return "ce_rows";
     case FLCE_KERNEL_ZERO: return "zero";
+    case FLCE_KERNEL_BIAS_REDUCE: return "bias_reduce";
   }
   return "unknown";
 }

@@ -612,32 +612,44 @@ __device__ int cta_count_valid(const CeParams& p, int64_t t_first) {
 }
 
 // Single-launch form: the arrival counter that finds the last CTA needs no
-// zeroing beforehand.  Its 64-bit word holds (call nonce, CTAs arrived); CTA
-// 0 sets it to (nonce, 0) when it starts, and every CTA adds 1 when it ends.
-// An add that returns another tag came before that reset (which wiped it
-// out): the CTA waits for the reset to show, then adds again.  Returns the
-// number of CTAs arrived so far including this one (0 if the reset never
-// showed within the time limit; the status word then has the timeout bit).
-constexpr int kArrivalCountBits = 24;
-__device__ __forceinline__ unsigned long long arrival_tag(unsigned long long nonce) {
-  return nonce << kArrivalCountBits;
-}
-__device__ unsigned int arrive_tagged(unsigned long long* word, unsigned long long nonce, int* status) {
-  const unsigned long long tag = arrival_tag(nonce);
-  const unsigned long long mask = (1ull << kArrivalCountBits) - 1;
-  for (int attempt = 0; attempt < 4; ++attempt) {
-    const unsigned long long old = atomicAdd(word, 1ull);
-    if ((old & ~mask) == tag) return static_cast<unsigned int>((old & mask) + 1);
-    const uint64_t t0 = global_timer_ns();
-    while ((ld_relaxed_u64(word) & ~mask) != tag) {
-      if (global_timer_ns() - t0 > 2000000000ull) {
-        if (status != nullptr) atomicOr(status, FLCE_STATUS_BIT_TIMEOUT);
-        return 0;
-      }
-      __nanosleep(256);
-    }
+// zeroing beforehand.  Its 64-bit word holds (call nonce, CTAs arrived).  A
+// CTA adds 1 and reads back the old word; if it carries this call's tag, its
+// count is the CTA's draw.  Otherwise the word is still an older call's (or
+// whatever the memory held): the CTA replaces it by (nonce, 1) with a
+// compare-and-swap, its draw being 0, unless another CTA installed the tag
+// first, in which case it adds again.  No CTA ever waits for another to make
+// progress, so nothing assumes that the grid's CTAs run at the same time.
+// CTA 0 installs the tag (count 0) when it starts, so that the arrivals
+// normally take one atomic each.  The CAS loop only repeats when another CTA
+// changed the word meanwhile, at most once per CTA of the call; its bound is
+// a safeguard (status timeout bit, and a draw past every valid count).
+__device__ __forceinline__ unsigned long long tag_of(unsigned long long nonce) { return nonce << kTagCountBits; }
+
+// `old` is the value atomicAdd(word, 1) returned.
+__device__ unsigned int tagged_draw(unsigned long long* word, unsigned long long nonce, unsigned long long old,
+                                    int* status) {
+  const unsigned long long tag = tag_of(nonce);
+  const unsigned long long mask = (1ull << kTagCountBits) - 1;
+  if ((old & ~mask) == tag) return static_cast<unsigned int>(old & mask);
+  unsigned long long cur = old + 1;  // the word after this CTA's add
+  for (int i = 0; i < (1 << 20); ++i) {
+    if ((cur & ~mask) == tag) return static_cast<unsigned int>(atomicAdd(word, 1ull) & mask);
+    const unsigned long long prev = atomicCAS(word, cur, tag | 1ull);
+    if (prev == cur) return 0u;
+    cur = prev;
   }
-  return 0;  // not reached: the reset happens once per call
+  if (status != nullptr) atomicOr(status, FLCE_STATUS_BIT_TIMEOUT);
+  return static_cast<unsigned int>(mask);
+}
+
+// Puts this call's tag on the word (count 0) unless it is there already: one
+// read and one compare-and-swap whose result is not waited for.  If the swap
+// fails, another CTA changed the word first: either it installed the tag, or
+// its add hit the old tag and it installs the tag itself (tagged_draw).
+__device__ __forceinline__ void tagged_install(unsigned long long* word, unsigned long long nonce) {
+  const unsigned long long tag = tag_of(nonce);
+  const unsigned long long cur = ld_relaxed_u64(word);
+  if ((cur & ~((1ull << kTagCountBits) - 1)) != tag) atomicCAS(word, cur, tag);
 }
 
 // Sum / mean: the CTA's loss partial goes to loss_rows[blockIdx.x] and the
@@ -654,7 +666,9 @@ __device__ void ce_finish_loss(const CeParams& p, float part, int nv) {
   if (lane == 0) {
     p.loss_rows[blockIdx.x] = part;
     __threadfence();
-    arrived = p.done_flags == nullptr ? atomicAdd(p.ticket, 1u) + 1u : arrive_tagged(p.done_flags, p.nonce, p.status);
+    arrived = p.done_flags == nullptr
+                  ? atomicAdd(p.ticket, 1u) + 1u
+                  : tagged_draw(p.done_flags, p.nonce, atomicAdd(p.done_flags, 1ull), p.status) + 1u;
   }
   if (__shfl_sync(0xffffffffu, arrived, 0) != static_cast<unsigned int>(grid)) return;
   __threadfence();
@@ -683,11 +697,24 @@ constexpr int kRingGroups = 2;
 constexpr int kGroupThreads = kRingThreads / kRingGroups;
 constexpr int kGroupWarps = kGroupThreads / 32;
 
+// The row ring's barriers.  Buffer b has two, and its use u (the u-th load
+// into it) completes phase u / 2 of barrier full[2 b + u % 2].  With an odd
+// ring depth consecutive uses of a buffer go to different groups, so a group
+// may start waiting for use u while use u - 1 (the other group's) is still
+// landing; on a single barrier the parity of that wait could not tell the
+// two phases apart and the wait would pass early.  On alternating barriers
+// the previous phase of the one waited on is use u - 2, which this same
+// group has already consumed.
+__device__ __forceinline__ uint32_t ring_bar(const uint64_t* full, int bi, int use) {
+  return smem_addr(&full[2 * bi + (use & 1)]);
+}
+__device__ __forceinline__ uint32_t ring_parity(int use) { return static_cast<uint32_t>((use >> 1) & 1); }
+
 template <typename T, int VPT, bool UNAL>
 __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeParams p, int depth) {
   constexpr int EPV = 16 / sizeof(T);
   extern __shared__ __align__(128) uint8_t ring_smem[];
-  __shared__ uint64_t full[kRingMaxDepth];
+  __shared__ uint64_t full[2 * kRingMaxDepth];  // two per buffer, alternating by use (ring_bar)
   __shared__ int s_issued[kRingMaxDepth];  // loads issued into each buffer so far
   __shared__ float2 s_part[kRingGroups][2][kGroupWarps];  // per warp (max, sum of exp(z - max))
   __shared__ int s_abort;
@@ -708,7 +735,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < depth; ++i) {
-      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&full[2 * i]), 1);
+      mbar_init(smem_addr(&full[2 * i + 1]), 1);
       s_issued[i] = 0;
     }
     s_abort = 0;
@@ -725,30 +753,33 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   // that sees it waits for this copy
   auto issue = [&](int bi, int row) {
     volatile int* cnt = s_issued;
-    cnt[bi] = cnt[bi] + 1;
+    const int use = cnt[bi];
+    cnt[bi] = use + 1;
+    const uint32_t bar = ring_bar(full, bi, use);
     if constexpr (UNAL) {
       const RowSpan sp = row_span<T>(row, row_bytes, tail_limit);
       const uint32_t bytes = static_cast<uint32_t>(sp.nld) * 16u;
-      mbar_arrive_expect_tx(smem_addr(&full[bi]), bytes);
-      bulk_load(ring_base + bi * buf_stride, static_cast<const uint8_t*>(p.logits) + sp.a0, bytes, smem_addr(&full[bi]));
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_load(ring_base + bi * buf_stride, static_cast<const uint8_t*>(p.logits) + sp.a0, bytes, bar);
     } else {
-      mbar_arrive_expect_tx(smem_addr(&full[bi]), row_bytes);
+      mbar_arrive_expect_tx(bar, row_bytes);
       bulk_load(ring_base + bi * buf_stride, static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.V,
-                row_bytes, smem_addr(&full[bi]));
+                row_bytes, bar);
     }
   };
-  // waits (bounded) for the latest copy issued into every buffer
+  // waits (bounded) for the latest copy issued into every buffer (an earlier
+  // use of a buffer was consumed before the latest was issued)
   auto drain = [&]() {
     volatile int* cnt = s_issued;
     for (int bi = 0; bi < depth; ++bi) {
       const int c = cnt[bi];
-      if (c > 0) mbar_wait_drain(smem_addr(&full[bi]), static_cast<uint32_t>((c - 1) & 1), 2000000000ull);
+      if (c > 0) mbar_wait_drain(ring_bar(full, bi, c - 1), ring_parity(c - 1), 2000000000ull);
     }
   };
   const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < first && i < mine; ++i) issue(i, blockIdx.x + i * stride);
-    if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+    if (blockIdx.x == 0 && p.done_flags != nullptr) tagged_install(p.done_flags, p.nonce);
     if (blockIdx.x == 0 && p.clear_status) *p.status = 0;  // before this CTA flags anything
   }
   const bool full_rows = !UNAL && nvec == VPT * kGroupThreads;  // no vector past the row's end
@@ -764,14 +795,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   // before its data is waited for
   int iter = 0;
   for (int j = grp; j < mine; j += kRingGroups, ++iter) {
-    const int b = j % depth;
-    const uint32_t parity = static_cast<uint32_t>((j / depth) & 1);
+    const int b = j % depth, use = j / depth;
     const int row = blockIdx.x + j * stride;
     const int64_t t = __ldg(p.target + row);
     const float go = p.grad_out != nullptr ? __ldg(p.grad_out + row) : 1.f;
     // on a timeout the row is computed from whatever is in the buffer and
     // dropped at the group barrier below, which is also the abort vote
-    const bool ok = mbar_wait_sleep(smem_addr(&full[b]), parity, ctl);
+    const bool ok = mbar_wait_sleep(ring_bar(full, b, use), ring_parity(use), ctl);
     if (j == 0 && gtid == 0)  // group 0's first row is here: request the rest of the ring
       for (int i = first; i < depth && i < mine; ++i) issue(i, blockIdx.x + i * stride);
     // vectors past the row's end hold -inf: they add nothing to the max or the
@@ -995,7 +1025,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) ce_rows_stream_kernel(const
   const int64_t t_first = p.self_count && threadIdx.x < p.N ? __ldg(p.target + threadIdx.x) : 0;
   if (threadIdx.x == 0) {
     s_gsum = s_gcomp = 0.f;
-    if (blockIdx.x == 0 && p.done_flags != nullptr) st_relaxed_u64(p.done_flags, arrival_tag(p.nonce));
+    if (blockIdx.x == 0 && p.done_flags != nullptr) tagged_install(p.done_flags, p.nonce);
     if (blockIdx.x == 0 && p.clear_status) *p.status = 0;  // before this CTA flags anything
   }
   int nv = 1;

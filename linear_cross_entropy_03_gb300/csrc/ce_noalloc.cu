@@ -11,11 +11,15 @@
 // library holds until the process exits.  The caller passes only inputs and
 // outputs.
 //
-// The array is found with cudaGetSymbolAddress once per device, by the first
-// call made with that device current.  Every call shares the array: calls
-// that overlap on the GPU (different streams without ordering) race on it.
+// The array is found with cudaGetSymbolAddress once per device context, by
+// the first call made with that device current (again after a
+// cudaDeviceReset, whose new context holds the array at a new address).
+// Every call shares the array: calls that overlap on the GPU (different
+// streams without ordering) race on it.
 #include <atomic>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "flce_internal.h"
 
@@ -27,30 +31,68 @@ int64_t ce_vector_elems(int dtype, bool vector_path);
 namespace {
 
 constexpr size_t kHeaderBytes = 256;  // WorkspaceHeader, rounded up
-constexpr size_t kArrivalWordOffset = 192;  // the single-launch form's tagged counter, inside the header bytes
+constexpr size_t kArrivalWordOffset = 192;  // the single-launch form's tagged arrival counter
 static_assert(sizeof(flce::WorkspaceHeader) <= kArrivalWordOffset, "header overlaps the arrival word");
 constexpr size_t kScratchBytes = kHeaderBytes + sizeof(float) * FLCE_NOALLOC_MAX_ROWS;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[64] = {nullptr};
+struct ScratchSlot {
+  unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+  void* addr;
+};
+ScratchSlot g_scratch[64] = {};
 
-// Device address of the array for the current device (host code cannot use
-// the symbol itself as an address).
+// Unique id of the calling thread's current context (0 if unavailable), from
+// the driver entry points the runtime hands out.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array in the current device's context (host code
+// cannot use the symbol itself as an address): looked up the first time a
+// context is seen, then reused while that context lives.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = p;
-  }
-  return g_scratch_addr[dev];
+  ScratchSlot& slot = g_scratch[dev];
+  const unsigned long long ctx = current_context_id();  // 0 before the runtime set up this thread's context
+  if (ctx != 0 && slot.ctx_id == ctx && slot.addr != nullptr) return slot.addr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  slot.addr = p;
+  slot.ctx_id = current_context_id();  // the lookup has made the device's context current
+  return slot.addr;
 }
 
 bool aligned_to(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// A 40-bit tag no earlier call of this process gave the shared array's
+// counters.
+unsigned long long next_nonce() {
+  static std::atomic<unsigned long long> nonce{0x7F4A7C159E3779B9ull};
+  return (nonce.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
+}
 int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
@@ -91,7 +133,6 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
     // one launch: the row kernel counts the targets itself and finds the CTA
     // that adds the loss partials by a nonce-tagged counter in the scratch
     // header, so nothing needs zeroing first
-    static std::atomic<unsigned long long> nonce{0x7F4A7C159E3779B9ull};
     CeParams p = {};
     p.logits = logits;
     p.grad = grad_logits;
@@ -109,7 +150,7 @@ extern "C" flce_status_t ce_fwd_bwd_noalloc(const void* logits, int dtype, void*
     p.loss_out = reduction != FLCE_REDUCTION_NONE ? loss : nullptr;
     p.self_count = 1;
     p.done_flags = reinterpret_cast<unsigned long long*>(scratch + kArrivalWordOffset);
-    p.nonce = (nonce.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
+    p.nonce = next_nonce();
     return launch_ce_rows(p, dtype, vec, ptrs16, false, stream) == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
   }
 

@@ -13,16 +13,11 @@ namespace flce {
 constexpr int kBM = 128;          // tile rows (tensor-memory lanes)
 constexpr int kBN = 256;          // tile columns (fp32 accumulator columns)
 constexpr int kBK = 64;           // k per pipeline stage (128 bytes of bf16)
-constexpr int kStages = 4;        // TMA -> MMA pipeline depth
 constexpr int kEpiWarps = 4;      // warps that drain the accumulators
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffering)
 constexpr int kTileRing = 8;      // scheduler ring of tile ids
 constexpr int kBoxBytes = 64 * 64 * 2;             // one TMA box: 64 x 64 bf16
-constexpr int kStageBytesA = kBM * kBK * 2;        // 16 KB
-constexpr int kStageBytesB = kBN * kBK * 2;        // 32 KB
-constexpr int kStageBytes = kStageBytesA + kStageBytesB;
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
 
 enum GemmMode { kModeForward = 0, kModeBackward = 1 };
 
@@ -49,6 +44,15 @@ struct GemmParams {
   float* tgt_logit;         // [c_len]
   // operands: 0 bf16, 1 fp16 (hidden, weight, bias, chunk logits, grad_hidden)
   int in_fp16;
+  // fp32 operands split into bf16 hi + lo planes (nseg = 3; else 1 or 0):
+  // every product is hi.hi + hi.lo + lo.hi, three segments of the k loop,
+  // each reading the hi or lo map of an operand; the chunk logits are
+  // stored as two planes z_plane elements apart (the upper and lower halves
+  // of their fp32 bits) and their gradient comes back as bf16 hi + lo
+  // planes at the same places; the bias is added in fp32 from bias_f32
+  int nseg;
+  int64_t z_plane;
+  const float* bias_f32;
   // fp16 only: dZ is stored divided by the uniform part of the row scale
   // (see uniform_scale), which the backward epilogue multiplies back in
   const int* n_valid;
@@ -91,9 +95,21 @@ struct RowParams {
   uint16_t* zbuf;           // chunk logits, bf16 or (z_fp16) fp16
   int64_t ldz;
   float* grad_bias;         // [V] or null
+  // with grad_bias: the column sums of each block of gl_rows rows go to
+  // bias_part [ceil(c_len / gl_rows), ldz] (fp32), then one thread per column
+  // adds them to grad_bias in block order (deterministic)
+  float* bias_part;
+  int gl_rows;
   int z_fp16;
+  // split fp32 operands: the chunk logits are two planes z_plane elements
+  // apart (upper and lower halves of their fp32 bits); dZ goes back to the
+  // same places as bf16 hi + lo planes.  0: one 16-bit plane
+  int64_t z_plane;
   const float* gmax;        // fp16: max |grad_out| over valid rows (reduction none)
 };
+
+// Rows per block of the grad-logits pass when it also sums the bias gradient.
+constexpr int kGlBiasRows = 128;
 
 struct CeParams {
   const void* logits;
@@ -116,13 +132,17 @@ struct CeParams {
   int64_t v_offset;         // global id of this shard's first column
   // single-launch form (no count kernel, nothing zeroed beforehand): every CTA
   // counts the valid targets itself, and the last CTA to finish is found by
-  // an arrival counter that CTA 0 tags with this call's nonce, instead of a
-  // zeroed ticket
+  // an arrival counter tagged with this call's nonce, instead of a zeroed
+  // ticket
   int self_count;
-  unsigned long long* done_flags;  // the tagged counter (one word), or null: use `ticket`
-  unsigned long long nonce;        // below 2^40, different from the previous call's
+  unsigned long long* done_flags;  // the tagged arrival counter (one word), or null: use `ticket`
+  unsigned long long nonce;        // below 2^40, different from every earlier call's on this memory
   int clear_status;                // CTA 0 zeroes *status when it starts (the workspace's own word)
 };
+
+// The tagged arrival counter: the low kTagCountBits bits of the 64-bit word
+// count, the bits above hold the call's nonce.
+constexpr int kTagCountBits = 24;
 
 // Most rows the single-launch CE form takes (each CTA reads every target).
 constexpr int64_t kCeSelfCountMaxRows = 16384;
@@ -165,10 +185,11 @@ cudaError_t launch_count_targets(const int64_t* target, int64_t N, int64_t V, in
                                  WorkspaceHeader* hdr, int num_counters, int zero_header,
                                  int* status, int32_t* n_valid_out, float* zero_a, int64_t zero_a_n,
                                  const float* grad_out, cudaStream_t s);
-cudaError_t launch_gemm(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
+// tm_h2 / tm_w2 / tm_z2: the lo planes of split fp32 operands (p.nseg = 3), else null
 cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w,
-                         const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s);
+                         const CUtensorMap& tm_z, const GemmParams& p, int grid, cudaStream_t s,
+                         const CUtensorMap* tm_h2 = nullptr, const CUtensorMap* tm_w2 = nullptr,
+                         const CUtensorMap* tm_z2 = nullptr);
 cudaError_t launch_row_finalize(const RowParams& p, cudaStream_t s);
 cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s);
 cudaError_t launch_vp_finalize(const RowParams& p, float* lse_out, float* lse16_out, float* zt_out,
@@ -180,6 +201,7 @@ cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction,
                                float* loss, cudaStream_t s, bool pdl);
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_f32_split_bf16(const float* in, uint16_t* hi, uint16_t* lo, int64_t n, cudaStream_t s);
 // vector_path: rows are whole 16-byte vectors and both pointers 16-byte
 // aligned; aligned_ptrs: both pointers 16-byte aligned (rows of any length).
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool aligned_ptrs, bool pdl,
@@ -189,7 +211,6 @@ cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool 
 bool ce_rows_single_launch_ok(int64_t V, int dtype, bool vector_path, bool aligned_ptrs);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 
-int gemm_max_smem_ok();  // sets kernel attributes once per device; 0 on failure
 int device_sm_count();
 
 // ---------------------------------------------------------------- profiler

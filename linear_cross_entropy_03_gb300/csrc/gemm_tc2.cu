@@ -1,13 +1,15 @@
 // Tensor-core contractions of the fused linear cross entropy, CTA-pair form.
 //
-// Same three products as gemm_tc.cu (torchtune post "Peak Performance,
-// Minimized Memory ...", Figure 1 "Fused Linear Cross Entropy", steps 2 and
-// 4) on 256 x 256 tiles computed by a pair of CTAs on two SMs with
-// tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and 128 columns of
-// B in its own shared memory, the pair's tensor cores read both halves, and
-// each CTA's tensor memory receives its 128 rows of the accumulator.  Per SM
-// this halves the operand bytes that TMA writes into shared memory and the
-// MMA reads back out, which is what limits the one-CTA 128 x 256 form.
+// The three products (torchtune post "Peak Performance, Minimized Memory
+// ...", Figure 1 "Fused Linear Cross Entropy", steps 2 and 4): the chunk
+// projection Z = H_c W^T with its cross-entropy epilogue, grad_H = dZ W and
+// grad_W += dZ^T H_c, on 256 x 256 tiles computed by a pair of CTAs on two
+// SMs with tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and 128
+// columns of B in its own shared memory, the pair's tensor cores read both
+// halves, and each CTA's tensor memory receives its 128 rows of the
+// accumulator.  Per SM this halves the operand bytes that TMA writes into
+// shared memory and the MMA reads back out, which limits a one-CTA
+// 128 x 256 form (measured at 71 % tensor-pipe busy against 83 % here).
 //
 // Roles (same in both CTAs unless noted):
 //   warp 0    TMA producer for this CTA's halves; in the leader CTA (rank 0)
@@ -63,7 +65,7 @@ __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams&
     const int gm = min(kFGroup, p.f_num_m - grp * kFGroup);
     ti.m0 = (grp * kFGroup + r % gm) * 256;
     ti.n0 = (r / gm) * kBN;
-    ti.kblocks = p.f_kblocks;
+    ti.kblocks = p.f_kblocks * (p.nseg > 1 ? p.nseg : 1);
   } else if (t < p.h_tiles) {
     // grad_H tiles (K = V, long) in groups of kHGroup row tiles, columns
     // varying within a group: the pairs running at once share fewer rows of
@@ -74,7 +76,7 @@ __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams&
     const int gm = min(kHGroup, p.h_num_m - grp * kHGroup);
     ti.m0 = (grp * kHGroup + r % gm) * 256;
     ti.n0 = (r / gm) * kWide;
-    ti.kblocks = p.h_kblocks;
+    ti.kblocks = p.h_kblocks * (p.nseg > 1 ? p.nseg : 1);
   } else {
     // grad_W tiles in groups of kWGroup hidden-column tiles, vocabulary rows
     // varying slowest within a group: the columns of H_c in use stay in L2
@@ -86,7 +88,7 @@ __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams&
     const int gn = min(kWGroup, p.w_num_n - grp * kWGroup);
     ti.n0 = (grp * kWGroup + r % gn) * kBN;
     ti.m0 = (r / gn) * 256;
-    ti.kblocks = p.w_kblocks;
+    ti.kblocks = p.w_kblocks * (p.nseg > 1 ? p.nseg : 1);
   }
   return ti;
 }
@@ -138,8 +140,10 @@ __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias,
 
 // Epilogue of one tile for this warp's 32 accumulator rows (`rl` = row
 // within the pair tile of this thread).  F16: fp16 operands (chunk logits and
-// grad_hidden in fp16); out_scale multiplies the backward products.
-template <bool F16>
+// grad_hidden in fp16); SPLIT: fp32 operands as bf16 hi + lo planes (chunk
+// logits stored exactly, as the two halves of their fp32 bits; fp32 bias);
+// out_scale multiplies the backward products.
+template <bool F16, bool SPLIT>
 __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl,
                                               float out_scale) {
   if (ti.kind == 0) {
@@ -162,10 +166,22 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
       const int lim = ncols - c;
-      if (p.bias != nullptr) add_bias32<F16>(x, p.bias + ti.n0 + c, lim);
+      if (SPLIT) {
+        if (p.bias_f32 != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < lim) x[j] += __ldg(p.bias_f32 + ti.n0 + c + j);
+        }
+      } else if (p.bias != nullptr) {
+        add_bias32<F16>(x, p.bias + ti.n0 + c, lim);
+      }
+      // the 16-bit logits (SPLIT: the upper halves of the fp32 bits, the
+      // lower halves going to the second plane)
       uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) pk[i] = pack16<F16>(x[2 * i], x[2 * i + 1]);
+      for (int i = 0; i < 16; ++i)
+        pk[i] = SPLIT ? __byte_perm(__float_as_uint(x[2 * i]), __float_as_uint(x[2 * i + 1]), 0x7632)
+                      : pack16<F16>(x[2 * i], x[2 * i + 1]);
       float cmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -178,11 +194,11 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
       for (int i = 0; i < 16; ++i) {
         if (2 * i < lim) {
           s32 += __expf(x[2 * i] - m_new);
-          s16 += __expf(lo16<F16>(pk[i]) - m_new);
+          if (!SPLIT) s16 += __expf(lo16<F16>(pk[i]) - m_new);
         }
         if (2 * i + 1 < lim) {
           s32 += __expf(x[2 * i + 1] - m_new);
-          s16 += __expf(hi16<F16>(pk[i]) - m_new);
+          if (!SPLIT) s16 += __expf(hi16<F16>(pk[i]) - m_new);
         }
       }
       m_run = m_new;
@@ -199,8 +215,20 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
           if (8 * g4 < lim)
             __stcs(reinterpret_cast<uint4*>(zrow + c + 8 * g4),
                    make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]));
+        if (SPLIT) {  // the lower halves of the fp32 bits, one plane further
+          uint32_t lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            lo[i] = __byte_perm(__float_as_uint(x[2 * i]), __float_as_uint(x[2 * i + 1]), 0x5410);
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4)
+            if (8 * g4 < lim)
+              __stcs(reinterpret_cast<uint4*>(zrow + p.z_plane + c + 8 * g4),
+                     make_uint4(lo[4 * g4], lo[4 * g4 + 1], lo[4 * g4 + 2], lo[4 * g4 + 3]));
+        }
       }
     }
+    if (SPLIT) s16 = s32;  // the gradient is formed from the exact fp32 logits
     if (row_ok) p.partials[static_cast<int64_t>(r) * p.nvt + ti.n0 / kBN] = make_float4(m_run, s32, s16, 0.f);
   } else if (ti.kind == 1) {
     const int r = ti.m0 + rl;
@@ -267,7 +295,9 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-                 const __grid_constant__ CUtensorMap tm_z, const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_h2,
+                 const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_z2,
+                 const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -307,6 +337,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_h);
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_z);
+    if (p.nseg > 1) {
+      tma_prefetch_desc(&tm_h2);
+      tma_prefetch_desc(&tm_w2);
+      tma_prefetch_desc(&tm_z2);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
@@ -377,32 +412,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = sa + kHalf * kBK * 2;
           const uint32_t fb = map_to_cta(smem_addr(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), ti.kind == 1 ? 6 * kBoxBytes * 2 : 4 * kBoxBytes * 2);
-          const int k0 = kb * kBK;
+          // k block kb: with split fp32 operands the three segments
+          // (hi.hi, hi.lo, lo.hi) of each 64-wide k slice follow one another,
+          // so the hi tile a segment re-reads is still in L2
+          const int ns = p.nseg > 1 ? p.nseg : 1;
+          const int seg = kb % ns;
+          const int k0 = (kb / ns) * kBK;
+          // segment 0 multiplies A hi by B hi, 1 A hi by B lo, 2 A lo by B hi;
+          // H is A of the forward and B of grad_W, W is B, dZ is A
+          const bool h_lo = ti.kind == 0 ? seg == 2 : seg == 1;
+          const CUtensorMap* m_h = h_lo ? &tm_h2 : &tm_h;
+          const CUtensorMap* m_w = seg == 1 ? &tm_w2 : &tm_w;
+          const CUtensorMap* m_z = seg == 2 ? &tm_z2 : &tm_z;
           if (ti.kind == 0) {
             // the chunk's hidden rows are re-read by every vocabulary tile; the
             // weight is streamed once per chunk
             const int r = static_cast<int>(p.row0) + mh;
-            tma_load_2d_pair_hint(sa, &tm_h, fb, k0, r, pol_keep);
-            tma_load_2d_pair_hint(sa + kBoxBytes, &tm_h, fb, k0, r + 64, pol_keep);
-            tma_load_2d_pair_hint(sb, &tm_w, fb, k0, nh, pol_stream);
-            tma_load_2d_pair_hint(sb + kBoxBytes, &tm_w, fb, k0, nh + 64, pol_stream);
+            tma_load_2d_pair_hint(sa, m_h, fb, k0, r, pol_keep);
+            tma_load_2d_pair_hint(sa + kBoxBytes, m_h, fb, k0, r + 64, pol_keep);
+            tma_load_2d_pair_hint(sb, m_w, fb, k0, nh, pol_stream);
+            tma_load_2d_pair_hint(sb + kBoxBytes, m_w, fb, k0, nh + 64, pol_stream);
           } else if (ti.kind == 1) {
             // wide tile: this CTA's 128 columns of each 256-column half of B
-            tma_load_2d_pair(sa, &tm_z, fb, k0, mh);
-            tma_load_2d_pair(sa + kBoxBytes, &tm_z, fb, k0, mh + 64);
-            tma_load_2d_pair(sb, &tm_w, fb, nh, k0);
-            tma_load_2d_pair(sb + kBoxBytes, &tm_w, fb, nh + 64, k0);
-            tma_load_2d_pair(sb + 2 * kBoxBytes, &tm_w, fb, nh + kBN, k0);
-            tma_load_2d_pair(sb + 3 * kBoxBytes, &tm_w, fb, nh + kBN + 64, k0);
+            tma_load_2d_pair(sa, m_z, fb, k0, mh);
+            tma_load_2d_pair(sa + kBoxBytes, m_z, fb, k0, mh + 64);
+            tma_load_2d_pair(sb, m_w, fb, nh, k0);
+            tma_load_2d_pair(sb + kBoxBytes, m_w, fb, nh + 64, k0);
+            tma_load_2d_pair(sb + 2 * kBoxBytes, m_w, fb, nh + kBN, k0);
+            tma_load_2d_pair(sb + 3 * kBoxBytes, m_w, fb, nh + kBN + 64, k0);
           } else {
             // grad_W: every tile re-reads the chunk's hidden rows (kept in L2);
             // each dZ column panel serves only the tiles of one vocabulary row
             // running side by side (streamed)
-            tma_load_2d_pair_hint(sa, &tm_z, fb, mh, k0, pol_stream);
-            tma_load_2d_pair_hint(sa + kBoxBytes, &tm_z, fb, mh + 64, k0, pol_stream);
+            tma_load_2d_pair_hint(sa, m_z, fb, mh, k0, pol_stream);
+            tma_load_2d_pair_hint(sa + kBoxBytes, m_z, fb, mh + 64, k0, pol_stream);
             const int r = static_cast<int>(p.row0) + k0;
-            tma_load_2d_pair_hint(sb, &tm_h, fb, nh, r, pol_keep);
-            tma_load_2d_pair_hint(sb + kBoxBytes, &tm_h, fb, nh + 64, r, pol_keep);
+            tma_load_2d_pair_hint(sb, m_h, fb, nh, r, pol_keep);
+            tma_load_2d_pair_hint(sb + kBoxBytes, m_h, fb, nh + 64, r, pol_keep);
           }
           fills ^= 1u << stage;
           if (++stage == nst) stage = 0;
@@ -532,10 +578,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after_sync();
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+        const int rl = kHalf * static_cast<int>(rank) + q * 32 + lane;
         if (p.in_fp16)
-          epilogue_tile<true>(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane, out_scale);
+          epilogue_tile<true, false>(ti, p, tbase, rl, out_scale);
+        else if (p.nseg > 1)
+          epilogue_tile<false, true>(ti, p, tbase, rl, 1.f);
         else
-          epilogue_tile<false>(ti, p, tbase, kHalf * static_cast<int>(rank) + q * 32 + lane, 1.f);
+          epilogue_tile<false, false>(ti, p, tbase, rl, 1.f);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);
@@ -575,13 +624,16 @@ int gemm2_max_smem_ok() {
 
 // grid: number of CTAs, even (two per tile pair).
 cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& tm_w, const CUtensorMap& tm_z,
-                         const GemmParams& p, int grid, cudaStream_t s) {
+                         const GemmParams& p, int grid, cudaStream_t s, const CUtensorMap* tm_h2,
+                         const CUtensorMap* tm_w2, const CUtensorMap* tm_z2) {
   if (!gemm2_max_smem_ok()) return cudaErrorInvalidConfiguration;
   prof_begin(s, mode == kModeForward ? FLCE_KERNEL_GEMM_FWD : FLCE_KERNEL_GEMM_BWD);
   if (mode == kModeForward)
-    gemm2_kernel<kModeForward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
+    gemm2_kernel<kModeForward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(
+        tm_h, tm_w, tm_z, tm_h2 ? *tm_h2 : tm_h, tm_w2 ? *tm_w2 : tm_w, tm_z2 ? *tm_z2 : tm_z, p);
   else
-    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, p);
+    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(
+        tm_h, tm_w, tm_z, tm_h2 ? *tm_h2 : tm_h, tm_w2 ? *tm_w2 : tm_w, tm_z2 ? *tm_z2 : tm_z, p);
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;

@@ -141,11 +141,13 @@ __global__ void __launch_bounds__(32 * kFinalizeWarps) row_finalize_kernel(const
 
 constexpr int kGlThreads = 256;
 constexpr int kGlCols = kGlThreads * 8;  // one 16-byte vector of bf16 per thread
-constexpr int kGlRows = 32;              // rows per block (bias column sums)
+constexpr int kGlRows = 32;              // rows per block without the bias gradient
 constexpr int kGlUnroll = 4;
+static_assert(kGlBiasRows >= kGlRows && kGlBiasRows % kGlUnroll == 0, "grad-logits row blocks");
 
 // F16: fp16 chunk logits; dZ is stored divided by the rows' common scale
-// (uniform_scale), which the backward products multiply back in.
+// (uniform_scale), which the backward products multiply back in.  SPLIT:
+// exact fp32 chunk logits in two planes, dZ written back as bf16 hi + lo.
 template <bool F16>
 __device__ __forceinline__ float z_lo(uint32_t w) {
   return F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu))) : bf16_lo(w);
@@ -163,22 +165,29 @@ __device__ __forceinline__ uint32_t z_pack(float lo, float hi) {
   return pack_bf16x2(lo, hi);
 }
 
-template <bool F16>
+// d rounded to bf16 (nearest even) and the rounded remainder: d = hi + lo to
+// about 2^-16 of |d|.
+__device__ __forceinline__ void split_bf16(float d0, float d1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(d0, d1);
+  lo = pack_bf16x2(d0 - bf16_lo(hi), d1 - bf16_hi(hi));
+}
+
+template <bool F16, bool SPLIT>
 __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams p) {
-  __shared__ float s_lse[kGlRows], s_scale[kGlRows];
-  __shared__ int s_tgt[kGlRows];
+  __shared__ float s_lse[kGlBiasRows], s_scale[kGlBiasRows];
+  __shared__ int s_tgt[kGlBiasRows];
   grid_dependency_wait();
-  const int r0 = blockIdx.y * kGlRows;
-  const int rows = min(kGlRows, p.c_len - r0);
-  if (threadIdx.x < rows) {
-    s_lse[threadIdx.x] = p.row_lse[r0 + threadIdx.x];
-    s_scale[threadIdx.x] = p.row_scale[r0 + threadIdx.x];
+  const int r0 = blockIdx.y * p.gl_rows;
+  const int rows = min(p.gl_rows, p.c_len - r0);
+  for (int i = threadIdx.x; i < rows; i += kGlThreads) {
+    s_lse[i] = p.row_lse[r0 + i];
+    s_scale[i] = p.row_scale[r0 + i];
     if (p.row_tgt != nullptr) {
-      s_tgt[threadIdx.x] = p.row_tgt[r0 + threadIdx.x];
+      s_tgt[i] = p.row_tgt[r0 + i];
     } else {  // vocabulary shard: the target's column here, or -1 if another shard holds it
-      const int64_t tg = p.target[p.row0 + r0 + threadIdx.x];
+      const int64_t tg = p.target[p.row0 + r0 + i];
       const int64_t tl = tg - p.v_offset;
-      s_tgt[threadIdx.x] = (tg != p.ignore_index && tl >= 0 && tl < p.V) ? static_cast<int>(tl) : -1;
+      s_tgt[i] = (tg != p.ignore_index && tl >= 0 && tl < p.V) ? static_cast<int>(tl) : -1;
     }
   }
   __syncthreads();
@@ -195,31 +204,43 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
   for (int j = 0; j < 8; ++j) cs[j] = 0.f;
   uint16_t* base = p.zbuf + static_cast<int64_t>(r0) * p.ldz + v0;
   for (int rr = 0; rr < rows; rr += kGlUnroll) {
-    uint4 in[kGlUnroll];
+    uint4 in[kGlUnroll], in_lo[SPLIT ? kGlUnroll : 1];
 #pragma unroll
     for (int u = 0; u < kGlUnroll; ++u) {
-      if (rr + u < rows && s_scale[rr + u] != 0.f)
-        in[u] = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(rr + u) * p.ldz));
-      else
-        in[u] = make_uint4(0, 0, 0, 0);
+      const bool live = rr + u < rows && s_scale[rr + u] != 0.f;
+      const uint16_t* src = base + static_cast<int64_t>(rr + u) * p.ldz;
+      in[u] = live ? __ldcs(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+      if (SPLIT) in_lo[u] = live ? __ldcs(reinterpret_cast<const uint4*>(src + p.z_plane)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kGlUnroll; ++u) {
       const int r = rr + u;
       if (r >= rows) break;
       uint4* dst = reinterpret_cast<uint4*>(base + static_cast<int64_t>(r) * p.ldz);
+      uint4* dst_lo = SPLIT ? reinterpret_cast<uint4*>(base + static_cast<int64_t>(r) * p.ldz + p.z_plane) : nullptr;
       const int t = s_tgt[r];  // -1: no target column in this block of the vocabulary
       if (s_scale[r] == 0.f) {  // ignored row (or zero upstream gradient): exact zeros
         __stcs(dst, make_uint4(0, 0, 0, 0));
+        if (SPLIT) __stcs(dst_lo, make_uint4(0, 0, 0, 0));
         continue;
       }
       const float lse = s_lse[r], sc = s_scale[r];
       const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
       float d[8];
+      if (SPLIT) {  // the exact fp32 logits from their two halves
+        const uint32_t wl[4] = {in_lo[SPLIT ? u : 0].x, in_lo[SPLIT ? u : 0].y, in_lo[SPLIT ? u : 0].z,
+                                in_lo[SPLIT ? u : 0].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        d[2 * i] = z_lo<F16>(w[i]);
-        d[2 * i + 1] = z_hi<F16>(w[i]);
+        for (int i = 0; i < 4; ++i) {
+          d[2 * i] = __uint_as_float(__byte_perm(wl[i], w[i], 0x5410));
+          d[2 * i + 1] = __uint_as_float(__byte_perm(wl[i], w[i], 0x7632));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          d[2 * i] = z_lo<F16>(w[i]);
+          d[2 * i + 1] = z_hi<F16>(w[i]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -228,18 +249,44 @@ __global__ void __launch_bounds__(kGlThreads) grad_logits_kernel(const RowParams
         if (j < nval) cs[j] += d[j];
       }
       uint4 o;
-      o.x = z_pack<F16>(store_mul * d[0], store_mul * d[1]);
-      o.y = z_pack<F16>(store_mul * d[2], store_mul * d[3]);
-      o.z = z_pack<F16>(store_mul * d[4], store_mul * d[5]);
-      o.w = z_pack<F16>(store_mul * d[6], store_mul * d[7]);
+      if (SPLIT) {
+        uint4 ol;
+        split_bf16(d[0], d[1], o.x, ol.x);
+        split_bf16(d[2], d[3], o.y, ol.y);
+        split_bf16(d[4], d[5], o.z, ol.z);
+        split_bf16(d[6], d[7], o.w, ol.w);
+        __stcs(dst_lo, ol);
+      } else {
+        o.x = z_pack<F16>(store_mul * d[0], store_mul * d[1]);
+        o.y = z_pack<F16>(store_mul * d[2], store_mul * d[3]);
+        o.z = z_pack<F16>(store_mul * d[4], store_mul * d[5]);
+        o.w = z_pack<F16>(store_mul * d[6], store_mul * d[7]);
+      }
       __stcs(dst, o);
     }
   }
-  if (p.grad_bias != nullptr) {
+  if (p.grad_bias != nullptr) {  // this block's column sums; bias_reduce adds the blocks in order
+    float* dst = p.bias_part + static_cast<int64_t>(blockIdx.y) * p.ldz + v0;
+    if (nval == 8) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < nval) atomicAdd(p.grad_bias + v0 + j, cs[j]);
+      for (int j = 0; j < 8; ++j)
+        if (j < nval) dst[j] = cs[j];
+    }
   }
+}
+
+// grad_bias[v] += sum over row blocks b (in order) of part[b, v]: one thread
+// per column, so the sum's order is fixed and the result the same every run.
+__global__ void __launch_bounds__(256) bias_reduce_kernel(const float* __restrict__ part, int blocks, int64_t ld,
+                                                          int64_t V, float* __restrict__ grad_bias) {
+  const int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (v >= V) return;
+  float acc = 0.f;
+  for (int b = 0; b < blocks; ++b) acc += part[static_cast<int64_t>(b) * ld + v];
+  grad_bias[v] += acc;
 }
 
 // Per-row partials of one vocabulary shard after its forward products:
@@ -355,6 +402,32 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restric
     out[i] = static_cast<uint16_t>(pack_bf16x2(in[i], 0.f) & 0xFFFFu);
 }
 
+// fp32 -> bf16 hi + lo planes: hi = x rounded to bf16 (nearest even), lo =
+// (x - hi) rounded likewise, so hi + lo equals x to about 2^-16 of |x|.
+// 8 elements per thread and step, scalar tail; pointers 16-byte aligned.
+__global__ void __launch_bounds__(256) f32_split_bf16_kernel(const float* __restrict__ in, uint16_t* __restrict__ hi,
+                                                             uint16_t* __restrict__ lo, int64_t n) {
+  const int64_t n8 = n / 8;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += step) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(in) + 2 * i);
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(in) + 2 * i + 1);
+    uint4 h, l;
+    split_bf16(a.x, a.y, h.x, l.x);
+    split_bf16(a.z, a.w, h.y, l.y);
+    split_bf16(b.x, b.y, h.z, l.z);
+    split_bf16(b.z, b.w, h.w, l.w);
+    reinterpret_cast<uint4*>(hi)[i] = h;
+    reinterpret_cast<uint4*>(lo)[i] = l;
+  }
+  for (int64_t i = n8 * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += step) {
+    uint32_t h, l;
+    split_bf16(in[i], 0.f, h, l);
+    hi[i] = static_cast<uint16_t>(h & 0xFFFFu);
+    lo[i] = static_cast<uint16_t>(l & 0xFFFFu);
+  }
+}
+
 constexpr int kReduceThreads = 1024;
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -454,14 +527,22 @@ cudaError_t launch_row_finalize(const RowParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_grad_logits(const RowParams& p, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((p.V + kGlCols - 1) / kGlCols),
-                  static_cast<unsigned>((p.c_len + kGlRows - 1) / kGlRows));
-  prof_begin(s, FLCE_KERNEL_GRAD_LOGITS);
   RowParams pc = p;
+  pc.gl_rows = p.grad_bias != nullptr ? kGlBiasRows : kGlRows;
+  const int row_blocks = (p.c_len + pc.gl_rows - 1) / pc.gl_rows;
+  const dim3 grid(static_cast<unsigned>((p.V + kGlCols - 1) / kGlCols), static_cast<unsigned>(row_blocks));
+  prof_begin(s, FLCE_KERNEL_GRAD_LOGITS);
   void* args[] = {&pc};
-  const void* fn = p.z_fp16 ? reinterpret_cast<const void*>(grad_logits_kernel<true>)
-                            : reinterpret_cast<const void*>(grad_logits_kernel<false>);
-  const cudaError_t e = launch_pdl(fn, grid, dim3(kGlThreads), args, s, false);
+  const void* fn = p.z_fp16    ? reinterpret_cast<const void*>(grad_logits_kernel<true, false>)
+                   : p.z_plane ? reinterpret_cast<const void*>(grad_logits_kernel<false, true>)
+                               : reinterpret_cast<const void*>(grad_logits_kernel<false, false>);
+  cudaError_t e = launch_pdl(fn, grid, dim3(kGlThreads), args, s, false);
+  prof_end(s);
+  if (e != cudaSuccess || p.grad_bias == nullptr) return e;
+  prof_begin(s, FLCE_KERNEL_BIAS_REDUCE);
+  bias_reduce_kernel<<<static_cast<unsigned>((p.V + 255) / 256), 256, 0, s>>>(p.bias_part, row_blocks, p.ldz, p.V,
+                                                                            p.grad_bias);
+  e = cudaGetLastError();
   prof_end(s);
   return e;
 }
@@ -530,6 +611,16 @@ cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaSt
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   f32_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_split_bf16(const float* in, uint16_t* hi, uint16_t* lo, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n / 8 + 255) / 256;
+  const int64_t cap = 8LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  f32_split_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(in, hi, lo, n);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ def host(t) -> np.ndarray:
 
 def run_flce(inp, *, reduction="mean", chunk=0, use_bias=True, grad_scale=1.0, grad_out=None,
              accumulate=False, grad_weight_init=None, grad_bias_init=None, ignore_index=None,
-             grads=True, keep_f32=False):
+             grads=True, keep_f32=False, fp32_mode="split"):
     h = dev16(inp.hidden)
     w = dev16(inp.weight)
     b = dev16(inp.bias) if (use_bias and inp.bias is not None) else None
@@ -47,7 +47,7 @@ def run_flce(inp, *, reduction="mean", chunk=0, use_bias=True, grad_scale=1.0, g
         h, w, t, b, ignore_index=inp.ignore_index if ignore_index is None else ignore_index,
         reduction=reduction, chunk=chunk, grad_scale=grad_scale, grad_out=go, grad_hidden=grads,
         grad_weight=grads, grad_weight_out=gw0, grad_bias_out=gb0 if b is not None else None,
-        accumulate=accumulate, row_stats=True)
+        accumulate=accumulate, row_stats=True, fp32_mode=fp32_mode)
     torch.cuda.synchronize()
     conv = (lambda x: x.float().cpu().numpy()) if keep_f32 else host
     res = {k: (conv(v) if isinstance(v, torch.Tensor) and k not in ("status", "n_valid", "workspace") else v)

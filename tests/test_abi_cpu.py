@@ -84,8 +84,16 @@ def test_flce_typed_workspace_holds_fp32_copies(lib):
     base = flce.flce_workspace_size(n, h, v, 0, "mean")
     assert flce.flce_workspace_size_typed("bf16", n, h, v, 0, "mean") == base
     assert flce.flce_workspace_size_typed("fp16", n, h, v, 0, "mean") == base
+    # rounded fp32 operands: one bf16 copy of hidden, weight and bias
+    f32r = flce.flce_workspace_size_typed("fp32_rounded", n, h, v, 0, "mean")
+    assert base + 2 * (n * h + v * h + v) <= f32r <= base + 2 * (n * h + v * h + v) + 3 * 256 + 2 * 64
+    # split fp32 operands: bf16 hi + lo planes of hidden and weight, and a
+    # second plane of chunk logits (the lower halves of their fp32 bits)
     f32 = flce.flce_workspace_size_typed("fp32", n, h, v, 0, "mean")
-    assert base + 2 * (n * h + v * h + v) <= f32 <= base + 2 * (n * h + v * h + v) + 3 * 256 + 2 * 64
+    chunk = flce.flce_default_chunk(n, h, v)
+    vp = -(-v // 8) * 8
+    extra = 4 * (n * h + v * h) + 2 * chunk * vp
+    assert base + extra - 256 <= f32 <= base + extra + 4 * 256  # (256-byte rounding of each region)
     assert flce.flce_workspace_size_typed(7, n, h, v, 0, "mean") == 0
     assert flce.flce_workspace_size_typed("fp32", -1, h, v, 0, "mean") == 0
 

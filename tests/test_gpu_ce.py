@@ -177,3 +177,28 @@ def test_ce_status_in_workspace_when_no_status_word():
         assert st == 0
         word = int(ws[:4].view(torch.int32).item())
         assert word == (0x1 if bad else 0), hex(word)
+
+
+@pytest.mark.parametrize("n,v", [(1024, 32768), (600, 128256), (20000, 256)])
+def test_ce_beside_kernels_holding_sms(n, v):
+    # The single-launch form finds its last CTA with a counter that no CTA
+    # waits on (a CTA that finds an older call's tag installs this call's
+    # itself), so it must give the same result when another stream's kernels
+    # hold part of the SMs while its CTAs start: a bounded bf16 matmul
+    # launched just before, on a second stream.
+    logits, t = si.make_ce_logits(n, v, 700 + n, std=2.0, dtype="bf16", ignore_frac=0.05)
+    ref = O.ce_reference(logits, t, reduction="mean")
+    side = torch.cuda.Stream()
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    tt = torch.from_numpy(t).cuda()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        z = dev_bf16(logits)
+        with torch.cuda.stream(side):
+            for _ in range(4):
+                a = (a @ a).clamp_(-1.0, 1.0)
+        out = flce.cross_entropy(z, tt, reduction="mean", in_place=True)
+        torch.cuda.synchronize()
+        assert int(out["status"].item()) == 0
+        assert_loss(host(out["loss"]), ref["loss"], "mean")
+        assert_grad(host(out["grad_logits"]), ref["dz"], "grad_logits")

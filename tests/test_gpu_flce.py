@@ -158,3 +158,4 @@ def test_repeated_calls_are_deterministic():
     assert a["loss"] == b["loss"]
     assert np.array_equal(a["grad_hidden"], b["grad_hidden"])
     assert np.array_equal(a["grad_weight"], b["grad_weight"])
+    assert np.array_equal(a["grad_bias"], b["grad_bias"])  # fixed-order column sums, no atomics

@@ -2,13 +2,10 @@
 bias (flce_fwd_bwd_typed, FLCE_DTYPE_FP16) against the fp64 oracle, which
 widens the same fp16 values exactly: every reduction, bias, ragged tails,
 chunking, accumulation, small upstream gradients (the fp16 grad-logits are
-stored relative to the rows' common scale) and a wider shape; plus the
-refusal of fp16 under the one-CTA GEMM form."""
+stored relative to the rows' common scale) and a wider shape."""
 import numpy as np
 import pytest
-import torch
 
-import linear_cross_entropy_03_gb300 as flce
 import synthetic_inputs as si
 from oracle import flce_oracle as O
 from gpu_util import assert_flce_parity, run_flce
@@ -67,13 +64,3 @@ def test_fp16_all_ignored_mean():
     res = run_flce(inp, reduction="mean", use_bias=False)
     assert res["n_valid"] == 0 and np.isnan(res["loss"])
     assert np.all(res["grad_hidden"] == 0.0) and np.all(res["grad_weight"] == 0.0)
-
-
-def test_fp16_refused_by_one_cta_form():
-    inp = si.make_flce_inputs(64, 64, 500, 91, dtype="fp16")
-    assert flce.flce_set_gemm_variant(flce.GEMM_SINGLE_CTA) == flce.GEMM_SINGLE_CTA
-    try:
-        with pytest.raises(flce.FlceError):
-            run_flce(inp, reduction="mean", use_bias=False)
-    finally:
-        flce.flce_set_gemm_variant(flce.GEMM_CTA_PAIR)

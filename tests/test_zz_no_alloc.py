@@ -15,40 +15,58 @@ import synthetic_inputs as si
 from gpu_util import assert_grad, assert_loss, dev_bf16, host
 
 
-def _with_workspace(z, t, n, v, reduction):
+def _dev(logits, dtype):
+    return dev_bf16(logits) if dtype == "bf16" else torch.from_numpy(logits).cuda()
+
+
+def _with_workspace(z, t, n, v, dtype, reduction, grad_out):
     grad = torch.empty_like(z)
     loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device="cuda")
-    ws_bytes = flce.ce_workspace_size(n, v, "bf16", reduction)
+    ws_bytes = flce.ce_workspace_size(n, v, dtype, reduction)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    st = flce.ce_fwd_bwd(z, "bf16", grad, t, n, v, -100, reduction, 1.0, None, loss, ws, ws_bytes, None)
+    st = flce.ce_fwd_bwd(z, dtype, grad, t, n, v, -100, reduction, 1.0, grad_out, loss, ws, ws_bytes, None)
     assert st == 0
     return loss, grad
 
 
-def _without_workspace(z, t, n, v, reduction):
+def _without_workspace(z, t, n, v, dtype, reduction, grad_out, with_status):
     grad = torch.empty_like(z)
     loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    st = flce.ce_fwd_bwd_noalloc(z, "bf16", grad, t, n, v, -100, reduction, 1.0, None, loss, status)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda") if with_status else None
+    st = flce.ce_fwd_bwd_noalloc(z, dtype, grad, t, n, v, -100, reduction, 1.0, grad_out, loss, status)
     assert st == 0
     return loss, grad, status
 
 
+# (n, v, seed, dtype, reduction, status word): one launch for N <= 16384 (row
+# ring up to 72 KB rows, streaming form beyond); the counting kernel + ticket
+# form for more rows, with both row forms
+CASES = [(1024, 32768, 1002, "bf16", "mean", True), (300, 5000, 7, "bf16", "sum", True),
+         (20000, 64, 9, "bf16", "mean", True), (513, 5003, 11, "bf16", "mean", True),
+         (700, 3000, 13, "bf16", "none", True), (400, 8192, 15, "bf16", "mean", False),
+         (256, 30000, 17, "fp32", "sum", True), (16400, 40000, 19, "bf16", "mean", True)]
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
-    # one launch for N <= 16384; the counting kernel + ticket form beyond
-    cases = [(si.make_ce_logits(1024, 32768, 1002), "mean"), (si.make_ce_logits(300, 5000, 7), "sum"),
-             (si.make_ce_logits(20000, 64, 9), "mean"), (si.make_ce_logits(513, 5003, 11), "mean")]
-    for (logits, tgt), reduction in cases:
-        n, v = logits.shape
-        z = dev_bf16(logits)
+    for n, v, seed, dtype, reduction, with_status in CASES:
+        logits, tgt = si.make_ce_logits(n, v, seed, dtype=dtype)
+        z = _dev(logits, dtype)
         t = torch.from_numpy(tgt).cuda()
-        ref_loss, ref_grad = _with_workspace(z, t, n, v, reduction)
-        loss, grad, status = _without_workspace(z, t, n, v, reduction)
-        torch.cuda.synchronize()
-        assert int(status.item()) == 0
-        assert_loss(host(loss)[0], host(ref_loss)[0], reduction)
-        assert_grad(host(grad), host(ref_grad), "grad_logits")
+        go = torch.from_numpy(si.make_grad_out(n, seed)).cuda() if reduction == "none" else None
+        ref_loss, ref_grad = _with_workspace(z, t, n, v, dtype, reduction, go)
+        for _ in range(2):  # the second call finds the first call's contents in the shared array
+            loss, grad, status = _without_workspace(z, t, n, v, dtype, reduction, go, with_status)
+            torch.cuda.synchronize()
+            if with_status:
+                assert int(status.item()) == 0
+            if reduction == "none":
+                assert_loss(host(loss), host(ref_loss), reduction)
+            else:
+                assert_loss(host(loss)[0], host(ref_loss)[0], reduction)
+            assert_grad(host(grad), host(ref_grad), "grad_logits")
+        del z, ref_grad, grad
+        torch.cuda.empty_cache()
 
 
 @pytest.mark.gpu
