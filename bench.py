@@ -286,10 +286,13 @@ class L2Emptier:
             self.sleep(200000)
 
 
-def time_call(flce, call, empty_l2, iters=20, kernels=("ce_rows",)):
-    """Median time of `call` with L2 emptied before each (library profiling
-    off), and median of the summed durations of its `kernels` (library
-    events, a separate loop; None when kernels is empty)."""
+def time_call(flce, call, empty_l2, iters=50, kernels=("ce_rows",)):
+    """Mean time of `call` with L2 emptied before each (library profiling
+    off), and mean of the summed durations of its `kernels` (library
+    events, a separate loop; None when kernels is empty).  The mean, not the
+    median: the GPU's event clock advances in steps of about 2 us, so a
+    single call of ~30 us reads one of two neighbouring steps, and only the
+    mean over many calls resolves the time between them."""
     import torch
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times, kernel = [], []
@@ -302,7 +305,7 @@ def time_call(flce, call, empty_l2, iters=20, kernels=("ce_rows",)):
         if i >= 3:
             times.append(a.elapsed_time(b))
     if not kernels:
-        return statistics.median(times), None
+        return statistics.mean(times), None
     for i in range(iters + 3):
         flce.flce_profile_enable(16)
         empty_l2(i)
@@ -312,7 +315,7 @@ def time_call(flce, call, empty_l2, iters=20, kernels=("ce_rows",)):
         flce.flce_profile_disable()
         if i >= 3:
             kernel.append(sum(ms for name, ms in rec if name in kernels))
-    return statistics.median(times), statistics.median(kernel)
+    return statistics.mean(times), statistics.mean(kernel)
 
 
 def ce_bandwidth(step, iters=20):

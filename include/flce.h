@@ -380,7 +380,8 @@ enum {
   FLCE_KERNEL_LOSS_REDUCE = 5,
   FLCE_KERNEL_CE_ROWS = 6,
   FLCE_KERNEL_ZERO = 7,
-  FLCE_KERNEL_BIAS_REDUCE = 8
+  FLCE_KERNEL_BIAS_REDUCE = 8,
+  FLCE_KERNEL_GH_REDUCE = 9
 };
 const char* flce_kernel_name(int kernel_id);
 flce_status_t flce_profile_enable(int capacity);

@@ -29,7 +29,7 @@ DTYPES = {"bf16": 0, "fp32": 1, "fp16": 2, "fp32_rounded": 3}
 STATUS_BIT_TARGET_RANGE = 0x1
 STATUS_BIT_TIMEOUT = 0x2
 KERNEL_NAMES = ("count_targets", "gemm_forward", "row_finalize", "grad_logits", "gemm_backward",
-                "loss_reduce", "ce_rows", "zero", "bias_reduce")
+                "loss_reduce", "ce_rows", "zero", "bias_reduce", "gh_reduce")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libflce03.so")

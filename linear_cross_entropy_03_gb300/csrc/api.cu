@@ -76,11 +76,25 @@ bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int6
 
 // ---------------------------------------------------------------- layouts
 struct FlceLayout {
-  int64_t chunk, num_chunks, vp, nvt;
-  size_t header, zbuf, partials, tgt_logit, row_lse, row_scale, row_tgt, loss_rows, total;
+  int64_t chunk, num_chunks, vp, nvt;  // nvt: 256-column vocabulary tiles
+  int64_t npart;                       // room for per-row LSE partials: one per kPartColsMin columns
+  int gh_slices;  // most K slices of a split grad_H (1: never split)
+  size_t header, zbuf, partials, tgt_logit, row_lse, row_scale, row_tgt, loss_rows, gh_part, total;
   size_t cvt_h, cvt_w, cvt_b;  // fp32 operands: their bf16 copies (0 bytes otherwise)
   int64_t z_plane;             // split fp32 operands: elements between the two chunk-logit planes (else 0)
 };
+
+// grad_H tiles (256 x 512, K = V) fewer than the SM pairs leave pairs idle
+// for the longest products of the backward launch: their K range is then
+// split into slices, as many as fill the pairs, each at least 8 k blocks
+// (512 of the vocabulary) long.
+constexpr int kGemmMaxPairs = 128;  // sizes the partial-sum buffer for any GPU up to 256 SMs
+int gh_slices(int64_t rows, int64_t H, int64_t V, int pairs) {
+  const int64_t base = ceil_div(rows, 2 * kBM) * ceil_div(H, 2 * kBN);
+  if (base <= 0 || base >= pairs) return 1;
+  const int64_t most = std::max<int64_t>(1, ceil_div(V, kBK) / 8);
+  return static_cast<int>(std::min<int64_t>(ceil_div(pairs, base), most));
+}
 
 int64_t default_chunk(int64_t N, int64_t V) {
   int64_t c = kDefaultChunkBudget / (V * 2);
@@ -101,6 +115,7 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   L->num_chunks = N > 0 ? ceil_div(N, L->chunk) : 0;
   L->vp = round_up(static_cast<size_t>(V), 8);
   L->nvt = ceil_div(V, kBN);
+  L->npart = ceil_div(V, kPartColsMin);
   size_t off = 0;
   L->header = off;
   off = round_up(off + sizeof(WorkspaceHeader) + sizeof(unsigned int) * 2 * (L->num_chunks + 1), kAlign);
@@ -116,7 +131,7 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   L->partials = off;
   // the per-tile partials of the forward epilogue; after row_finalize the same
   // bytes take the grad-logits pass's per-row-block bias column sums
-  off = round_up(off + std::max(static_cast<size_t>(L->chunk) * L->nvt * sizeof(float4),
+  off = round_up(off + std::max(static_cast<size_t>(L->chunk) * L->npart * sizeof(float4),
                                 static_cast<size_t>(ceil_div(L->chunk, kGlBiasRows)) * L->vp * sizeof(float)),
                  kAlign);
   L->tgt_logit = off;
@@ -129,6 +144,9 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   off = round_up(off + static_cast<size_t>(L->chunk) * 4, kAlign);
   L->loss_rows = off;
   off = round_up(off + (reduction == FLCE_REDUCTION_NONE ? 0 : static_cast<size_t>(N) * 4), kAlign);
+  L->gh_slices = gh_slices(L->chunk, H, V, kGemmMaxPairs);
+  L->gh_part = off;
+  off = round_up(off + (L->gh_slices > 1 ? static_cast<size_t>(L->gh_slices) * L->chunk * H * 4 : 0), kAlign);
   const size_t copies = split ? 2 : (rounded ? 1 : 0);
   L->cvt_h = off;
   off = round_up(off + copies * static_cast<size_t>(N) * H * 2, kAlign);
@@ -350,7 +368,8 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     g.zbuf = zbuf;
     g.ldz = L.vp;
     g.partials = partials;
-    g.nvt = static_cast<int>(L.nvt);
+    g.epi_warps = forward_epi_warps(H, g.nseg);
+    g.nvt = static_cast<int>(ceil_div(V, part_cols(g.epi_warps)));
     g.tgt_logit = tgt_logit;
     g.grad_hidden = fp32 ? nullptr : static_cast<uint16_t*>(grad_hidden);
     g.grad_hidden_f32 = fp32 ? static_cast<float*>(grad_hidden) : nullptr;
@@ -382,7 +401,7 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     r.grad_out = grad_out_none;
     r.target = target;
     r.partials = partials;
-    r.nvt = static_cast<int>(L.nvt);
+    r.nvt = g.nvt;
     r.tgt_logit = tgt_logit;
     r.n_valid = &hdr->n_valid;
     r.row_lse = row_lse;
@@ -405,8 +424,14 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
 
     g.h_num_m = static_cast<int>(ceil_div(c_len, tile_m));
     g.h_kblocks = static_cast<int>(ceil_div(V, kBK));
-    // grad_H in 256 x 512 tiles
-    g.h_tiles = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, 2 * kBN)) : 0;
+    // grad_H in 256 x 512 tiles, split along K when they are too few
+    g.h_base = grad_hidden != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, 2 * kBN)) : 0;
+    g.h_split = g.h_base > 0 ? std::min(gh_slices(c_len, H, V, sms / 2), L.gh_slices) : 1;
+    g.h_kbs = static_cast<int>(ceil_div(g.h_kblocks, g.h_split));
+    g.h_split = static_cast<int>(ceil_div(g.h_kblocks, g.h_kbs));  // no empty slice
+    g.h_tiles = g.h_base * g.h_split;
+    g.gh_part = g.h_split > 1 ? reinterpret_cast<float*>(ws + L.gh_part) : nullptr;
+    g.gh_part_ld = L.chunk * H;
     g.w_num_n = static_cast<int>(ceil_div(H, kBN));
     g.w_kblocks = static_cast<int>(ceil_div(c_len, kBK));
     const int w_tiles = grad_weight != nullptr ? static_cast<int>(ceil_div(V, tile_m) * g.w_num_n) : 0;
@@ -415,6 +440,10 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     if (g.num_tiles > 0)
       FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream,
                                  split ? &tm_h2 : nullptr, split ? &tm_w2 : nullptr, split ? &tm_z2 : nullptr));
+    if (g.h_tiles > 0 && g.h_split > 1)
+      FLCE_TRY_CUDA(launch_gh_reduce(g.gh_part, g.h_split, g.gh_part_ld, c_len, static_cast<int>(H), row0,
+                                     fp32 ? nullptr : static_cast<uint16_t*>(grad_hidden), fp16 ? 1 : 0,
+                                     fp32 ? static_cast<float*>(grad_hidden) : nullptr, stream));
   }
   if (reduction != FLCE_REDUCTION_NONE)
     FLCE_TRY_CUDA(launch_loss_reduce(loss_rows, N, reduction, &hdr->n_valid, loss, stream, false));
@@ -569,7 +598,8 @@ flce_status_t flce_vp_forward(const void* hidden, const void* weight_shard, cons
   g.zbuf = reinterpret_cast<uint16_t*>(ws + L.zbuf);
   g.ldz = L.vp;
   g.partials = reinterpret_cast<float4*>(ws + L.partials);
-  g.nvt = static_cast<int>(L.nvt);
+  g.epi_warps = forward_epi_warps(H, 1);
+  g.nvt = static_cast<int>(ceil_div(V_shard, part_cols(g.epi_warps)));
   g.tgt_logit = reinterpret_cast<float*>(ws + L.tgt_logit);
   g.status = status;
   g.timeout_ns = g_timeout_ns.load();
@@ -654,15 +684,23 @@ flce_status_t flce_vp_backward(const void* hidden, const void* weight_shard, con
   g.timeout_ns = g_timeout_ns.load();
   g.h_num_m = static_cast<int>(ceil_div(C, tile_m));
   g.h_kblocks = static_cast<int>(ceil_div(V_shard, kBK));
-  g.h_tiles =
-      grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, 2 * kBN)) : 0;
+  const int sms = device_sm_count();
+  g.h_base = grad_hidden_partial != nullptr ? static_cast<int>(g.h_num_m * ceil_div(H, 2 * kBN)) : 0;
+  g.h_split = g.h_base > 0 ? std::min(gh_slices(C, H, V_shard, sms / 2), L.gh_slices) : 1;
+  g.h_kbs = static_cast<int>(ceil_div(g.h_kblocks, g.h_split));
+  g.h_split = static_cast<int>(ceil_div(g.h_kblocks, g.h_kbs));
+  g.h_tiles = g.h_base * g.h_split;
+  g.gh_part = g.h_split > 1 ? reinterpret_cast<float*>(ws + L.gh_part) : nullptr;
+  g.gh_part_ld = L.chunk * H;
   g.w_num_n = static_cast<int>(ceil_div(H, kBN));
   g.w_kblocks = static_cast<int>(ceil_div(C, kBK));
   const int w_tiles = grad_weight_shard != nullptr ? static_cast<int>(ceil_div(V_shard, tile_m) * g.w_num_n) : 0;
   g.num_tiles = g.h_tiles + w_tiles;
   g.tile_counter = &hdr->tile_counters[1];
-  const int sms = device_sm_count();
   FLCE_TRY_CUDA(launch_gemm2(kModeBackward, tm_h, tm_w, tm_z, g, 2 * std::min(sms / 2, g.num_tiles), stream));
+  if (g.h_tiles > 0 && g.h_split > 1)
+    FLCE_TRY_CUDA(launch_gh_reduce(g.gh_part, g.h_split, g.gh_part_ld, static_cast<int>(C), static_cast<int>(H), 0,
+                                   nullptr, 0, grad_hidden_partial, stream));
   return FLCE_OK;
 }
 
@@ -751,6 +789,7 @@ const char* flce_kernel_name(int id) {
     case FLCE_KERNEL_CE_ROWS: return "ce_rows";
     case FLCE_KERNEL_ZERO: return "zero";
     case FLCE_KERNEL_BIAS_REDUCE: return "bias_reduce";
+    case FLCE_KERNEL_GH_REDUCE: return "gh_reduce";
   }
   return "unknown";
 }

@@ -856,7 +856,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       zt = own_t ? to_f<T>(reinterpret_cast<const T*>(ring_smem + b * buf_stride)[tcol]) : 0.f;
     }
     // warp max, then exp(z - warp max) in place and its warp sum
-    const float mw = warp_max(vec_max_all<T, VPT>(v, VPT, 1));
+    const float mw = warp_max_redux(vec_max_all<T, VPT>(v, VPT, 1));
     const float nm = mw > -INFINITY ? -mw * kLog2e : 0.f;  // a warp past the row's end: all -inf, sum 0
     const float2 nmL = make_float2(nm, nm);
     float2 acc = make_float2(0.f, 0.f);
@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     if (gtid == 0 && j + depth < mine) issue(b, row + depth * stride);
     // every warp combines the group's warp partials itself
     const float2 q = lane < kGroupWarps ? s_part[grp][iter & 1][lane] : make_float2(-INFINITY, 0.f);
-    const float M = warp_max(q.x);
+    const float M = warp_max_redux(q.x);
     const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
     const float lse = M + logf(S);
 

@@ -13,8 +13,15 @@ namespace flce {
 constexpr int kBM = 128;          // tile rows (tensor-memory lanes)
 constexpr int kBN = 256;          // tile columns (fp32 accumulator columns)
 constexpr int kBK = 64;           // k per pipeline stage (128 bytes of bf16)
-constexpr int kEpiWarps = 4;      // warps that drain the accumulators
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+// Warps that drain the accumulators: 4 (one per TMEM lane quarter) or 8 (two
+// per quarter, each taking half of a tile's columns), chosen per launch.
+constexpr int kEpiWarpsMax = 8;
+// columns of a tile one epilogue warp drains, and so of one LSE partial
+constexpr int part_cols(int epi_warps) { return kBN / (epi_warps / 4); }
+constexpr int kPartColsMin = part_cols(kEpiWarpsMax);  // 128
+// Forward launches use 8 epilogue warps when the k loop is short (H * nseg
+// below 4096), where draining a tile takes longer than its MMAs.
+inline int forward_epi_warps(int64_t H, int nseg) { return H * (nseg > 1 ? nseg : 1) < 4096 ? 8 : 4; }
 constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffering)
 constexpr int kTileRing = 8;      // scheduler ring of tile ids
 constexpr int kBoxBytes = 64 * 64 * 2;             // one TMA box: 64 x 64 bf16
@@ -33,14 +40,23 @@ struct GemmParams {
   // grad_W (M = vocabulary, N = H, K = chunk tokens)
   int h_tiles, h_num_m, h_kblocks;
   int w_num_n, w_kblocks;
+  // grad_H split along K (the vocabulary) when its tiles are fewer than the
+  // SM pairs: h_tiles = h_base * h_split tiles, slice s taking k blocks
+  // [s h_kbs, (s + 1) h_kbs); each slice writes fp32 partial sums to
+  // gh_part [h_split][chunk rows][H] (slice stride gh_part_ld elements),
+  // added in slice order by gh_reduce afterwards.  h_split 1: direct stores
+  int h_base, h_split, h_kbs;
+  float* gh_part;
+  int64_t gh_part_ld;
   // forward epilogue
   const uint16_t* bias;     // bf16 [V] or null
   const int64_t* target;    // [N]
   int64_t v_offset;         // global id of this weight's first vocabulary row (0 unless sharded)
   uint16_t* zbuf;           // bf16 [c_len, ldz] chunk logits
   int64_t ldz;
-  float4* partials;         // [c_len, nvt]: (max, sum exp(z - max), same over bf16(z), 0)
-  int nvt;
+  float4* partials;         // [c_len, nvt]: (max, sum exp(z - max), same over bf16(z), 0) per part_cols columns
+  int nvt;                  // partials per row: ceil(V / part_cols(epi_warps))
+  int epi_warps;            // 4 or 8 (forward_epi_warps); backward launches use 4
   float* tgt_logit;         // [c_len]
   // operands: 0 bf16, 1 fp16 (hidden, weight, bias, chunk logits, grad_hidden)
   int in_fp16;
@@ -202,6 +218,11 @@ cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction,
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
 cudaError_t launch_f32_split_bf16(const float* in, uint16_t* hi, uint16_t* lo, int64_t n, cudaStream_t s);
+// grad_H rows [row0, row0 + rows) (H columns) from the split-K partial sums
+// part [slices][rows][H] (slice stride `ld` elements), added in slice order:
+// out16 (bf16, or fp16 when f16) or out32 (fp32), whichever is not null.
+cudaError_t launch_gh_reduce(const float* part, int slices, int64_t ld, int rows, int H, int64_t row0,
+                             uint16_t* out16, int f16, float* out32, cudaStream_t s);
 // vector_path: rows are whole 16-byte vectors and both pointers 16-byte
 // aligned; aligned_ptrs: both pointers 16-byte aligned (rows of any length).
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool aligned_ptrs, bool pdl,

@@ -39,7 +39,9 @@ constexpr int kWideStages = 4;
 constexpr int kWideStageBytes = 3 * kHalf * kBK * 2;
 static_assert(kWideStages * kWideStageBytes <= kRingSlots * kNarrowStageBytes, "wide layout exceeds the ring");
 constexpr int kGemm2SmemBytes = kRingSlots * kNarrowStageBytes + 1024 + 1024;
-constexpr int kRingConsumers2 = 1 + kEpiWarps + 1 + kEpiWarps;  // leader MMA + epi, peer producer + epi
+// tile-ring consumers: leader MMA issuer + epilogue warps, peer producer + epilogue warps
+constexpr int ring_consumers(int epi_warps) { return 1 + epi_warps + 1 + epi_warps; }
+constexpr int gemm_threads(int epi_warps) { return 64 + 32 * epi_warps; }
 constexpr int kHGroup = 8;  // row tiles per group in the grad_H tile order
 constexpr int kFGroup = 16;  // row tiles per group in the forward tile order
 #ifndef FLCE_W_GROUP
@@ -50,11 +52,14 @@ constexpr int kWGroup = FLCE_W_GROUP;  // hidden-column tiles per group in the g
 struct Tile2 {
   int kind;  // 0 forward, 1 grad_H, 2 grad_W
   int m0, n0, kblocks;
+  int kb0, slice;  // first k block of the tile's K range (split grad_H tiles), and its slice
 };
 
 // Pair tiles: 256 rows of M, 256 columns of N.
 __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams& p) {
   Tile2 ti;
+  ti.kb0 = 0;
+  ti.slice = 0;
   if (mode == kModeForward) {
     // row tiles in groups of kFGroup (4096 tokens), vocabulary tiles varying
     // slowest within a group: the hidden rows in use stay resident in L2
@@ -70,13 +75,20 @@ __device__ __forceinline__ Tile2 decode_tile2(int mode, int t, const GemmParams&
     // grad_H tiles (K = V, long) in groups of kHGroup row tiles, columns
     // varying within a group: the pairs running at once share fewer rows of
     // dZ and columns of W, so fewer of them are re-read from DRAM
+    // (split along K: the slices of one output tile lie h_base tiles apart)
     ti.kind = 1;
-    const int per_group = kHGroup * (p.h_tiles / p.h_num_m);
-    const int grp = t / per_group, r = t % per_group;
+    const int split = p.h_split > 1 ? p.h_split : 1;
+    const int base = split > 1 ? p.h_base : p.h_tiles;
+    const int b = t % base;
+    ti.slice = t / base;
+    const int per_group = kHGroup * (base / p.h_num_m);
+    const int grp = b / per_group, r = b % per_group;
     const int gm = min(kHGroup, p.h_num_m - grp * kHGroup);
     ti.m0 = (grp * kHGroup + r % gm) * 256;
     ti.n0 = (r / gm) * kWide;
-    ti.kblocks = p.h_kblocks * (p.nseg > 1 ? p.nseg : 1);
+    const int kbs = split > 1 ? p.h_kbs : p.h_kblocks;
+    ti.kb0 = ti.slice * kbs;
+    ti.kblocks = (min(p.h_kblocks, ti.kb0 + kbs) - ti.kb0) * (p.nseg > 1 ? p.nseg : 1);
   } else {
     // grad_W tiles in groups of kWGroup hidden-column tiles, vocabulary rows
     // varying slowest within a group: the columns of H_c in use stay in L2
@@ -139,13 +151,16 @@ __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias,
 }
 
 // Epilogue of one tile for this warp's 32 accumulator rows (`rl` = row
-// within the pair tile of this thread).  F16: fp16 operands (chunk logits and
-// grad_hidden in fp16); SPLIT: fp32 operands as bf16 hi + lo planes (chunk
-// logits stored exactly, as the two halves of their fp32 bits; fp32 bias);
-// out_scale multiplies the backward products.
-template <bool F16, bool SPLIT>
+// within the pair tile of this thread) and its PC columns from c_lo (with 8
+// epilogue warps two share each TMEM lane quarter, one per half of the
+// columns; with 4, PC is the whole tile).
+// F16: fp16 operands (chunk logits and grad_hidden in fp16); SPLIT: fp32
+// operands as bf16 hi + lo planes (chunk logits stored exactly, as the two
+// halves of their fp32 bits; fp32 bias); out_scale multiplies the backward
+// products.
+template <bool F16, bool SPLIT, int PC>
 __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl,
-                                              float out_scale) {
+                                              int c_lo, float out_scale) {
   if (ti.kind == 0) {
     const int r = ti.m0 + rl;
     const bool row_ok = r < p.c_len;
@@ -157,7 +172,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
     }
     uint16_t* zrow = p.zbuf + static_cast<int64_t>(row_ok ? r : 0) * p.ldz + ti.n0;
     float m_run = -INFINITY, s32 = 0.f, s16 = 0.f;
-    for (int c = 0; c < kBN; c += 32) {
+    for (int c = c_lo; c < c_lo + PC; c += 32) {
       if (c >= ncols) break;
       uint32_t v[32];
       tmem_load_32cols(tbase + c, v);
@@ -229,19 +244,32 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
       }
     }
     if (SPLIT) s16 = s32;  // the gradient is formed from the exact fp32 logits
-    if (row_ok) p.partials[static_cast<int64_t>(r) * p.nvt + ti.n0 / kBN] = make_float4(m_run, s32, s16, 0.f);
+    if (row_ok && ti.n0 + c_lo < p.V)
+      p.partials[static_cast<int64_t>(r) * p.nvt + (ti.n0 + c_lo) / PC] = make_float4(m_run, s32, s16, 0.f);
   } else if (ti.kind == 1) {
     const int r = ti.m0 + rl;
     const bool row_ok = r < p.c_len;
     const int ncols = min(kBN, p.H - ti.n0);
     const int64_t off = (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
     uint16_t* out = p.grad_hidden + off;
-    for (int c = 0; c < kBN; c += 32) {
+    // a K slice of a split tile: its fp32 partial sums, scaled like the output
+    float* part = p.h_split > 1 ? p.gh_part + ti.slice * p.gh_part_ld +
+                                      static_cast<int64_t>(row_ok ? r : 0) * p.H + ti.n0
+                                : nullptr;
+    for (int c = c_lo; c < c_lo + PC; c += 32) {
       if (c >= ncols) break;
       uint32_t v[32];
       tmem_load_32cols(tbase + c, v);
       tmem_load_wait();
-      if (row_ok && p.grad_hidden_f32 != nullptr) {  // fp32 partial of a vocabulary shard
+      if (row_ok && part != nullptr) {
+        float4* o4 = reinterpret_cast<float4*>(part + c);
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4)
+          if (c + 4 * g4 < ncols)
+            __stcg(o4 + g4, make_float4(out_scale * __uint_as_float(v[4 * g4]), out_scale * __uint_as_float(v[4 * g4 + 1]),
+                                        out_scale * __uint_as_float(v[4 * g4 + 2]),
+                                        out_scale * __uint_as_float(v[4 * g4 + 3])));
+      } else if (row_ok && p.grad_hidden_f32 != nullptr) {  // fp32 output (fp32 operands, a shard's partial)
         float4* o4 = reinterpret_cast<float4*>(p.grad_hidden_f32 + off + c);
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4)
@@ -265,7 +293,7 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
     const bool row_ok = vrow < p.V;
     const int ncols = min(kBN, p.H - ti.n0);
     float* out = p.grad_weight + static_cast<int64_t>(row_ok ? vrow : 0) * p.H + ti.n0;
-    for (int c = 0; c < kBN; c += 32) {
+    for (int c = c_lo; c < c_lo + PC; c += 32) {
       if (c >= ncols) break;
       uint32_t v[32];
       tmem_load_32cols(tbase + c, v);
@@ -275,16 +303,13 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           if (c + 4 * g < ncols) {
-            float4 a = make_float4(out_scale * __uint_as_float(v[4 * g]), out_scale * __uint_as_float(v[4 * g + 1]),
-                                   out_scale * __uint_as_float(v[4 * g + 2]), out_scale * __uint_as_float(v[4 * g + 3]));
-            if (!p.gw_store) {  // read-add-write, streamed past L2's resident data
-              const float4 b = __ldcs(o4 + g);
-              a.x += b.x;
-              a.y += b.y;
-              a.z += b.z;
-              a.w += b.w;
-            }
-            __stcs(o4 + g, a);
+            const float4 a = make_float4(out_scale * __uint_as_float(v[4 * g]), out_scale * __uint_as_float(v[4 * g + 1]),
+                                         out_scale * __uint_as_float(v[4 * g + 2]),
+                                         out_scale * __uint_as_float(v[4 * g + 3]));
+            if (p.gw_store)
+              __stcs(o4 + g, a);
+            else  // one fire-and-forget add per element and launch: the L2 does the read-add-write
+              red_add_f32x4(o4 + g, a);
           }
         }
       }
@@ -292,8 +317,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
   }
 }
 
-template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+template <int MODE, int EW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_h2,
                  const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_z2,
@@ -325,11 +350,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_addr(&tfull[a]), 1);
-      mbar_init(smem_addr(&tempty[a]), 2 * kEpiWarps);
+      mbar_init(smem_addr(&tempty[a]), 2 * EW);
     }
     for (int i = 0; i < kTileRing; ++i) {
       mbar_init(smem_addr(&ring_full[i]), 1);
-      mbar_init(smem_addr(&ring_empty[i]), kRingConsumers2);
+      mbar_init(smem_addr(&ring_empty[i]), ring_consumers(EW));
     }
     mbar_init(smem_addr(done), 1);
     *abort_flag = 0;
@@ -417,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           // so the hi tile a segment re-reads is still in L2
           const int ns = p.nseg > 1 ? p.nseg : 1;
           const int seg = kb % ns;
-          const int k0 = (kb / ns) * kBK;
+          const int k0 = (ti.kb0 + kb / ns) * kBK;
           // segment 0 multiplies A hi by B hi, 1 A hi by B lo, 2 A lo by B hi;
           // H is A of the forward and B of grad_W, W is B, dZ is A
           const bool h_lo = ti.kind == 0 ? seg == 2 : seg == 1;
@@ -547,7 +572,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------ epilogue warps
-    const int q = warp & 3;
+    const int q = warp & 3;                                // TMEM lane quarter (hardware rule: warp % 4)
+    constexpr int PC = part_cols(EW);
+    const int c_lo = ((warp - 2) / 4) * PC;               // this warp's columns of every tile
     // fp16: the chunk's dZ was stored divided by the rows' common scale
     const float out_scale = (MODE == kModeBackward && p.in_fp16)
                                 ? uniform_scale(p.reduction, p.grad_scale, p.n_valid, p.gmax)
@@ -580,11 +607,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
         const int rl = kHalf * static_cast<int>(rank) + q * 32 + lane;
         if (p.in_fp16)
-          epilogue_tile<true, false>(ti, p, tbase, rl, out_scale);
+          epilogue_tile<true, false, PC>(ti, p, tbase, rl, c_lo, out_scale);
         else if (p.nseg > 1)
-          epilogue_tile<false, true>(ti, p, tbase, rl, 1.f);
+          epilogue_tile<false, true, PC>(ti, p, tbase, rl, c_lo, 1.f);
         else
-          epilogue_tile<false, false>(ti, p, tbase, rl, 1.f);
+          epilogue_tile<false, false, PC>(ti, p, tbase, rl, c_lo, 1.f);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);
@@ -612,10 +639,13 @@ int gemm2_max_smem_ok() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (configured[dev]) return 1;
-  if (cudaFuncSetAttribute(gemm2_kernel<kModeForward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm2_kernel<kModeForward, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kGemm2SmemBytes) != cudaSuccess)
     return 0;
-  if (cudaFuncSetAttribute(gemm2_kernel<kModeBackward>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm2_kernel<kModeForward, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGemm2SmemBytes) != cudaSuccess)
+    return 0;
+  if (cudaFuncSetAttribute(gemm2_kernel<kModeBackward, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kGemm2SmemBytes) != cudaSuccess)
     return 0;
   configured[dev] = 1;
@@ -628,12 +658,15 @@ cudaError_t launch_gemm2(int mode, const CUtensorMap& tm_h, const CUtensorMap& t
                          const CUtensorMap* tm_w2, const CUtensorMap* tm_z2) {
   if (!gemm2_max_smem_ok()) return cudaErrorInvalidConfiguration;
   prof_begin(s, mode == kModeForward ? FLCE_KERNEL_GEMM_FWD : FLCE_KERNEL_GEMM_BWD);
-  if (mode == kModeForward)
-    gemm2_kernel<kModeForward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(
-        tm_h, tm_w, tm_z, tm_h2 ? *tm_h2 : tm_h, tm_w2 ? *tm_w2 : tm_w, tm_z2 ? *tm_z2 : tm_z, p);
+  const CUtensorMap& h2 = tm_h2 ? *tm_h2 : tm_h;
+  const CUtensorMap& w2 = tm_w2 ? *tm_w2 : tm_w;
+  const CUtensorMap& z2 = tm_z2 ? *tm_z2 : tm_z;
+  if (mode == kModeForward && p.epi_warps == 8)
+    gemm2_kernel<kModeForward, 8><<<grid, gemm_threads(8), kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, h2, w2, z2, p);
+  else if (mode == kModeForward)
+    gemm2_kernel<kModeForward, 4><<<grid, gemm_threads(4), kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, h2, w2, z2, p);
   else
-    gemm2_kernel<kModeBackward><<<grid, kGemmThreads, kGemm2SmemBytes, s>>>(
-        tm_h, tm_w, tm_z, tm_h2 ? *tm_h2 : tm_h, tm_w2 ? *tm_w2 : tm_w, tm_z2 ? *tm_z2 : tm_z, p);
+    gemm2_kernel<kModeBackward, 4><<<grid, gemm_threads(4), kGemm2SmemBytes, s>>>(tm_h, tm_w, tm_z, h2, w2, z2, p);
   const cudaError_t e = cudaGetLastError();
   prof_end(s);
   return e;

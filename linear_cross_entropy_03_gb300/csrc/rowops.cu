@@ -428,6 +428,40 @@ __global__ void __launch_bounds__(256) f32_split_bf16_kernel(const float* __rest
   }
 }
 
+// grad_H from the split-K partial sums: 8 consecutive columns per thread and
+// step (H % 8 == 0), slices added in order (deterministic).
+__global__ void __launch_bounds__(256) gh_reduce_kernel(const float* __restrict__ part, int slices, int64_t ld,
+                                                        int rows, int H, int64_t row0, uint16_t* out16, int f16,
+                                                        float* out32) {
+  const int64_t n8 = static_cast<int64_t>(rows) * H / 8;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += step) {
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < slices; ++s) {
+      const float4* src = reinterpret_cast<const float4*>(part + s * ld) + 2 * i;
+      const float4 x = __ldcs(src), y = __ldcs(src + 1);
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+    const int64_t o = row0 * H + 8 * i;  // rows of the chunk lie row0 rows into the output
+    if (out32 != nullptr) {
+      reinterpret_cast<float4*>(out32 + o)[0] = make_float4(a[0], a[1], a[2], a[3]);
+      reinterpret_cast<float4*>(out32 + o)[1] = make_float4(a[4], a[5], a[6], a[7]);
+    } else if (f16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 h = __floats2half2_rn(a[2 * q], a[2 * q + 1]);
+        w[q] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(out16 + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      *reinterpret_cast<uint4*>(out16 + o) =
+          make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+    }
+  }
+}
+
 constexpr int kReduceThreads = 1024;
 
 __global__ void __launch_bounds__(kReduceThreads)
@@ -622,6 +656,20 @@ cudaError_t launch_f32_split_bf16(const float* in, uint16_t* hi, uint16_t* lo, i
   if (blocks < 1) blocks = 1;
   f32_split_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(in, hi, lo, n);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gh_reduce(const float* part, int slices, int64_t ld, int rows, int H, int64_t row0,
+                             uint16_t* out16, int f16, float* out32, cudaStream_t s) {
+  const int64_t n8 = static_cast<int64_t>(rows) * H / 8;
+  if (n8 <= 0) return cudaSuccess;
+  int64_t blocks = (n8 + 255) / 256;
+  const int64_t cap = 8LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  prof_begin(s, FLCE_KERNEL_GH_REDUCE);
+  gh_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(part, slices, ld, rows, H, row0, out16, f16, out32);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(s);
+  return e;
 }
 
 cudaError_t launch_loss_reduce(const float* loss_rows, int64_t N, int reduction, const int* n_valid,

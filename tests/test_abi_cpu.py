@@ -126,11 +126,14 @@ def test_workspace_grows_with_chunk_not_n_times_v(lib):
     n, v, h = e["batch"] * e["seq_len"], e["vocab"], 4096
     full_logits = n * v * e["bytes_per_logit"]                      # the 16.8 GB of the page
     ws = flce.flce_workspace_size(n, h, v, 2048, "sum")
-    assert 2048 * v * 2 <= ws <= 2048 * v * 2 * 1.05 + 4 * n + (1 << 20)
-    assert ws < full_logits / 15
+    # the chunk's bf16 logits, its per-row LSE partials (16 bytes per 128
+    # columns: 1/16 of the logits' bytes), O(N) per-row terms and, with
+    # 2048-token chunks, two K slices of grad_H partial sums (fp32 [2048, H] each)
+    assert 2048 * v * 2 <= ws <= 2048 * v * 2 * (1 + 1 / 16 + 0.01) + 4 * n + 2 * 2048 * h * 4 + (1 << 20)
+    assert ws < full_logits / 14
     ws2 = flce.flce_workspace_size(2 * n, h, v, 2048, "sum")
     assert ws2 - ws < 8 * n + 4096                                  # only O(N) per-row terms grow
-    assert flce.flce_workspace_size(n, h, v, 4096, "sum") > 1.9 * ws - (1 << 20)
+    assert flce.flce_workspace_size(n, h, v, 4096, "sum") > 1.8 * ws
     assert flce.flce_workspace_size(n, h, v, 2048, "none") < ws    # no per-row loss buffer
     assert flce.flce_workspace_size(-1, h, v, 0, "sum") == 0
     c = flce.flce_default_chunk(16384, 4096, 128256)

@@ -75,3 +75,31 @@ def test_noalloc_rejects_more_rows_than_its_scratch_holds():
     st = flce.ce_fwd_bwd_noalloc(0x10000, "bf16", None, 0x10000, n, 8, -100, "sum", 1.0, None, 0x10000,
                                  None, 0)
     assert st == 2  # FLCE_ERR_UNSUPPORTED, returned before anything is enqueued
+
+
+@pytest.mark.gpu
+def test_noalloc_calls_leave_free_device_memory_unchanged():
+    # every buffer is made first and every kernel form is loaded by a first
+    # round of calls; later calls must not change the device's free memory
+    forms = [(1024, 32768, 21, "bf16", "mean"), (64, 200000, 23, "bf16", "sum"), (20000, 64, 25, "bf16", "none")]
+    bufs = []
+    for n, v, seed, dtype, reduction in forms:
+        logits, tgt = si.make_ce_logits(n, v, seed, dtype=dtype)
+        z = _dev(logits, dtype)
+        t = torch.from_numpy(tgt).cuda()
+        go = torch.from_numpy(si.make_grad_out(n, seed)).cuda() if reduction == "none" else None
+        loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bufs.append((z, torch.empty_like(z), t, n, v, dtype, reduction, go, loss, status))
+
+    def call_all():
+        for z, grad, t, n, v, dtype, reduction, go, loss, status in bufs:
+            assert flce.ce_fwd_bwd_noalloc(z, dtype, grad, t, n, v, -100, reduction, 1.0, go, loss, status) == 0
+        torch.cuda.synchronize()
+
+    call_all()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        call_all()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert all(int(b[-1].item()) == 0 for b in bufs)
