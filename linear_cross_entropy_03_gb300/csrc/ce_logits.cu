@@ -358,6 +358,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 // Packet helpers of the row-ring form: a 16-byte vector of 8 bf16 / fp16 or 4 fp32.
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T>
 __device__ __forceinline__ float vec_max(const uint4& v);
@@ -672,8 +673,17 @@ __device__ void ce_finish_loss(const CeParams& p, float part, int nv) {
   }
   if (__shfl_sync(0xffffffffu, arrived, 0) != static_cast<unsigned int>(grid)) return;
   __threadfence();
+  // the lane's partials are loaded together (one memory latency, not one per
+  // load), then added in index order (a missing one adds an exact 0)
+  constexpr int kBatch = 8;
   float a = 0.f;
-  for (int i = lane; i < grid; i += 32) a += ld_relaxed_f32(p.loss_rows + i);
+  for (int i0 = lane; i0 < grid; i0 += 32 * kBatch) {
+    float x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) x[k] = i0 + 32 * k < grid ? ld_relaxed_f32(p.loss_rows + i0 + 32 * k) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) a += x[k];
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
   if (lane == 0) {
@@ -790,6 +800,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     grid_dependency_wait();  // n_valid and the zeroed ticket come from the count kernel
     if (p.reduction == FLCE_REDUCTION_MEAN) nv = *p.n_valid;
   }
+  // gradient scale of a valid row (times grad_out[row] for reduction none)
+  const float base_scale = p.reduction == FLCE_REDUCTION_MEAN ? p.grad_scale / static_cast<float>(nv) : p.grad_scale;
 
   // this group's rows: j = grp, grp + 2, ...; a row's scalars are loaded
   // before its data is waited for
@@ -876,7 +888,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
     const float2 q = lane < kGroupWarps ? s_part[grp][iter & 1][lane] : make_float2(-INFINITY, 0.f);
     const float M = warp_max_redux(q.x);
     const float S = warp_sum(q.x > -INFINITY ? q.y * ex2_approx((q.x - M) * kLog2e) : 0.f);
-    const float lse = M + logf(S);
+    const float lse = M + lg2_approx(S) * kLn2;  // S >= 1: the warp holding M adds exp(0)
 
     if (p.lse_out != nullptr) {  // partials of a vocabulary shard
       if (own_t) p.zt_out[row] = zt;
@@ -886,60 +898,53 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
       }
       continue;
     }
-    if (p.loss_out != nullptr) {  // sum / mean: the group adds its rows' losses in row order
-      if (own_t) {               // (ordered across rows by the group barriers)
-        const float y = (lse - zt) - s_gcomp[grp];
-        const float t2 = s_gsum[grp] + y;
-        s_gcomp[grp] = (t2 - s_gsum[grp]) - y;
-        s_gsum[grp] = t2;
-      }
-    } else {
+    if (p.loss_out == nullptr) {  // reduction none: the row's loss
       if (own_t) p.loss_rows[row] = lse - zt;
       if (!valid && gtid == 0) p.loss_rows[row] = 0.f;
     }
-    if (p.grad == nullptr) continue;
-
-    float scale = 0.f;
-    if (valid) {
-      if (p.reduction == FLCE_REDUCTION_MEAN)
-        scale = p.grad_scale / static_cast<float>(nv);
-      else if (p.reduction == FLCE_REDUCTION_SUM)
-        scale = p.grad_scale;
-      else
-        scale = p.grad_scale * go;
-    }
-    // softmax = exp(z - warp max) * exp(warp max - M) / S: one multiply per
-    // element; the target element is formed again in fp32 from its logit
-    const float factor = scale * ex2_approx((mw - M) * kLog2e) * __frcp_rn(S);
+    if (p.grad != nullptr) {
+      const float scale = valid ? (p.reduction == FLCE_REDUCTION_NONE ? base_scale * go : base_scale) : 0.f;
+      // softmax = exp(z - warp max) * exp(warp max - M) / S: one multiply per
+      // element; the target element is formed again in fp32 from its logit
+      const float factor = scale * ex2_approx((mw - M) * kLog2e) * rcp_approx(S);
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
-    if constexpr (UNAL) {
-      uint8_t* gb = static_cast<uint8_t*>(p.grad) + sp.a0;
+      for (int i = 0; i < VPT; ++i) vec_scale<T>(v[i], factor);
+      if constexpr (UNAL) {
+        uint8_t* gb = static_cast<uint8_t*>(p.grad) + sp.a0;
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int vi = i * kGroupThreads + gtid;
-        if (vi >= sp.nvr) continue;
-        const int lo = vi == 0 ? sp.lead : 0, hi = vi == sp.nvr - 1 ? sp.tail : EPV;
-        if (lo > 0 || hi < EPV)  // a vector shared with a neighbouring row: this row's elements only
-          store_elems<T>(reinterpret_cast<T*>(gb + 16ull * vi), v[i], lo, hi);
-        else
-          __stcs(reinterpret_cast<uint4*>(gb + 16ull * vi), v[i]);
-      }
-    } else {
-      uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + gtid;
-      if (full_rows) {
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
+        for (int i = 0; i < VPT; ++i) {
+          const int vi = i * kGroupThreads + gtid;
+          if (vi >= sp.nvr) continue;
+          const int lo = vi == 0 ? sp.lead : 0, hi = vi == sp.nvr - 1 ? sp.tail : EPV;
+          if (lo > 0 || hi < EPV)  // a vector shared with a neighbouring row: this row's elements only
+            store_elems<T>(reinterpret_cast<T*>(gb + 16ull * vi), v[i], lo, hi);
+          else
+            __stcs(reinterpret_cast<uint4*>(gb + 16ull * vi), v[i]);
+        }
       } else {
+        uint4* gvec = reinterpret_cast<uint4*>(static_cast<T*>(p.grad) + static_cast<int64_t>(row) * p.V) + gtid;
+        if (full_rows) {
 #pragma unroll
-        for (int i = 0; i < VPT; ++i)
-          if (i * kGroupThreads + gtid < nvec) __stcs(gvec + i * kGroupThreads, v[i]);
+          for (int i = 0; i < VPT; ++i) __stcs(gvec + i * kGroupThreads, v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < VPT; ++i)
+            if (i * kGroupThreads + gtid < nvec) __stcs(gvec + i * kGroupThreads, v[i]);
+        }
       }
+      // the target element, formed again in fp32 from its logit, replaces what
+      // the vector store above wrote there (same thread, so it lands last)
+      if (own_t)
+        static_cast<T*>(p.grad)[static_cast<int64_t>(row) * p.V + tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
     }
-    // the target element, formed again in fp32 from its logit, replaces what
-    // the vector store above wrote there (same thread, so it lands last)
-    if (own_t)
-      static_cast<T*>(p.grad)[static_cast<int64_t>(row) * p.V + tcol] = from_f<T>(scale * (__expf(zt - lse) - 1.f));
+    // sum / mean: the group adds its rows' losses in row order (ordered
+    // across rows by the group barriers), after the row's stores are issued
+    if (p.loss_out != nullptr && own_t) {
+      const float y = (lse - zt) - s_gcomp[grp];
+      const float t2 = s_gsum[grp] + y;
+      s_gcomp[grp] = (t2 - s_gsum[grp]) - y;
+      s_gsum[grp] = t2;
+    }
   }
   // the other group gave up: copies it would have consumed must land first
   if (gtid == 0 && *static_cast<volatile int*>(&s_abort)) drain();
