@@ -129,6 +129,8 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return pack_bf16x2(lo, hi);
 }
 
+constexpr float kLog2eF = 1.4426950408889634f;
+
 template <bool F16>
 __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias, int lim) {
   if (lim >= 32) {
@@ -197,26 +199,52 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
       for (int i = 0; i < 16; ++i)
         pk[i] = SPLIT ? __byte_perm(__float_as_uint(x[2 * i]), __float_as_uint(x[2 * i + 1]), 0x7632)
                       : pack16<F16>(x[2 * i], x[2 * i + 1]);
-      float cmax = -INFINITY;
+      if (lim >= 32) {
+        // a whole chunk: no per-column bounds, a three-input maximum tree,
+        // exp(z - m) as ex2 of one fused multiply-add, packed fp32x2
+        // arithmetic for two columns at a time, two independent sums
+        float m8[8];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < lim) cmax = fmaxf(cmax, x[j]);
-      const float m_new = fmaxf(m_run, cmax);
-      const float corr = __expf(m_run - m_new);
-      s32 *= corr;
-      s16 *= corr;
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[4 * i], x[4 * i + 1], fmax3(x[4 * i + 2], x[4 * i + 3], m_run));
+        const float m_new = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        const float corr = ex2_approx((m_run - m_new) * kLog2eF);  // 0 on the first chunk (m_run = -inf)
+        const float nmL = -m_new * kLog2eF;
+        const float2 l2e = make_float2(kLog2eF, kLog2eF), nm2 = make_float2(nmL, nmL);
+        float2 a32 = make_float2(0.f, 0.f), a16 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (2 * i < lim) {
-          s32 += __expf(x[2 * i] - m_new);
-          if (!SPLIT) s16 += __expf(lo16<F16>(pk[i]) - m_new);
+        for (int i = 0; i < 16; ++i) {
+          const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), l2e, nm2);
+          a32 = __fadd2_rn(a32, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+          if (!SPLIT) {
+            const float2 u = __ffma2_rn(make_float2(lo16<F16>(pk[i]), hi16<F16>(pk[i])), l2e, nm2);
+            a16 = __fadd2_rn(a16, make_float2(ex2_approx(u.x), ex2_approx(u.y)));
+          }
         }
-        if (2 * i + 1 < lim) {
-          s32 += __expf(x[2 * i + 1] - m_new);
-          if (!SPLIT) s16 += __expf(hi16<F16>(pk[i]) - m_new);
+        s32 = s32 * corr + (a32.x + a32.y);
+        s16 = s16 * corr + (a16.x + a16.y);
+        m_run = m_new;
+      } else {
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < lim) cmax = fmaxf(cmax, x[j]);
+        const float m_new = fmaxf(m_run, cmax);
+        const float corr = __expf(m_run - m_new);
+        s32 *= corr;
+        s16 *= corr;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (2 * i < lim) {
+            s32 += __expf(x[2 * i] - m_new);
+            if (!SPLIT) s16 += __expf(lo16<F16>(pk[i]) - m_new);
+          }
+          if (2 * i + 1 < lim) {
+            s32 += __expf(x[2 * i + 1] - m_new);
+            if (!SPLIT) s16 += __expf(hi16<F16>(pk[i]) - m_new);
+          }
         }
+        m_run = m_new;
       }
-      m_run = m_new;
       if (t_rel >= c && t_rel < c + 32) {
         float zt = 0.f;
 #pragma unroll
@@ -407,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
             break;
           }
           t = ring[slot];
-          mbar_arrive_cluster(map_to_cta(smem_addr(&ring_empty[slot]), 0));
+          mbar_arrive_remote(map_to_cta(smem_addr(&ring_empty[slot]), 0));
         }
         if (++slot == kTileRing) {
           slot = 0;
@@ -587,7 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
       if (!warp_wait_cluster(smem_addr(&ring_full[slot]), rphase, ctl)) break;
       const int t = ring[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_addr(&ring_empty[slot]), 0));
+      if (lane == 0) mbar_arrive_remote(map_to_cta(smem_addr(&ring_empty[slot]), 0));
       if (++slot == kTileRing) {
         slot = 0;
         rphase ^= 1u;
@@ -614,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
           epilogue_tile<false, false, PC>(ti, p, tbase, rl, c_lo, 1.f);
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_tempty0 : leader_tempty1);
+        if (lane == 0) mbar_arrive_remote(acc == 0 ? leader_tempty0 : leader_tempty1);
         if (++acc == 2) {
           acc = 0;
           aphase ^= 1u;
