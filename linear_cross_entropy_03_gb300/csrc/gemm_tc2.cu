@@ -162,14 +162,14 @@ __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias,
 // products.
 template <bool F16, bool SPLIT, int PC>
 __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl,
-                                              int c_lo, float out_scale) {
+                                              int c_lo, float out_scale, int64_t row_target) {
   if (ti.kind == 0) {
     const int r = ti.m0 + rl;
     const bool row_ok = r < p.c_len;
     const int ncols = min(kBN, p.V - ti.n0);
     int t_rel = -1;
     if (row_ok) {
-      const int64_t tg = p.target[p.row0 + r] - p.v_offset;
+      const int64_t tg = row_target - p.v_offset;
       if (tg >= ti.n0 && tg < ti.n0 + ncols) t_rel = static_cast<int>(tg - ti.n0);
     }
     uint16_t* zrow = p.zbuf + static_cast<int64_t>(row_ok ? r : 0) * p.ldz + ti.n0;
@@ -624,6 +624,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
       Tile2 ti = decode_tile2(MODE, t, p);
       // a wide grad_H tile arrives as two 256-column halves, one per buffer
       const int nbuf = ti.kind == 1 ? 2 : 1;
+      const int rl = kHalf * static_cast<int>(rank) + q * 32 + lane;
+      // forward: the row's target, loaded while the accumulator is computed
+      const int64_t row_target =
+          (MODE == kModeForward && ti.m0 + rl < p.c_len) ? __ldg(p.target + p.row0 + ti.m0 + rl) : 0;
       bool ok = true;
       for (int half = 0; half < nbuf; ++half) {
         if (!warp_wait_cluster(smem_addr(&tfull[acc]), aphase, ctl)) {
@@ -633,13 +637,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
         tc_fence_after_sync();
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-        const int rl = kHalf * static_cast<int>(rank) + q * 32 + lane;
         if (p.in_fp16)
-          epilogue_tile<true, false, PC>(ti, p, tbase, rl, c_lo, out_scale);
+          epilogue_tile<true, false, PC>(ti, p, tbase, rl, c_lo, out_scale, row_target);
         else if (p.nseg > 1)
-          epilogue_tile<false, true, PC>(ti, p, tbase, rl, c_lo, 1.f);
+          epilogue_tile<false, true, PC>(ti, p, tbase, rl, c_lo, 1.f, row_target);
         else
-          epilogue_tile<false, false, PC>(ti, p, tbase, rl, c_lo, 1.f);
+          epilogue_tile<false, false, PC>(ti, p, tbase, rl, c_lo, 1.f, row_target);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(acc == 0 ? leader_tempty0 : leader_tempty1);

@@ -437,7 +437,22 @@ __global__ void __launch_bounds__(256) gh_reduce_kernel(const float* __restrict_
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += step) {
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < slices; ++s) {
+    int s = 0;
+    for (; s + 4 <= slices; s += 4) {  // four slices' loads in flight, added in slice order
+      float4 x[4], y[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4* src = reinterpret_cast<const float4*>(part + (s + k) * ld) + 2 * i;
+        x[k] = __ldcs(src);
+        y[k] = __ldcs(src + 1);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[0] += x[k].x; a[1] += x[k].y; a[2] += x[k].z; a[3] += x[k].w;
+        a[4] += y[k].x; a[5] += y[k].y; a[6] += y[k].z; a[7] += y[k].w;
+      }
+    }
+    for (; s < slices; ++s) {
       const float4* src = reinterpret_cast<const float4*>(part + s * ld) + 2 * i;
       const float4 x = __ldcs(src), y = __ldcs(src + 1);
       a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
@@ -468,21 +483,33 @@ __global__ void __launch_bounds__(kReduceThreads)
     loss_reduce_kernel(const float* __restrict__ loss_rows, int64_t N, int reduction,
                        const int* n_valid, float* loss) {
   grid_dependency_wait();
-  double acc = 0.0;
-  for (int64_t i = threadIdx.x; i < N; i += kReduceThreads) acc += static_cast<double>(loss_rows[i]);
+  // each thread: a compensated fp32 sum of its rows in index order; then two
+  // fixed shuffle trees (warp, then block).  Deterministic, and accurate to
+  // about 1e-6 relative for any N (fp32 throughout: fp64 is slow here)
+  float sum = 0.f, comp = 0.f;
+  for (int64_t i = threadIdx.x; i < N; i += kReduceThreads) {
+    const float y = loss_rows[i] - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+  }
+  float acc = sum - comp;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  __shared__ double s_acc[kReduceThreads / 32];
+  __shared__ float s_acc[kReduceThreads / 32];
   if ((threadIdx.x & 31) == 0) s_acc[threadIdx.x >> 5] = acc;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double total = 0.0;
-    for (int w = 0; w < kReduceThreads / 32; ++w) total += s_acc[w];
-    if (reduction == FLCE_REDUCTION_MEAN) {
-      const int nv = *n_valid;
-      loss[0] = nv > 0 ? static_cast<float>(total / nv) : __int_as_float(0x7fc00000);
-    } else {
-      loss[0] = static_cast<float>(total);
+  if (threadIdx.x < 32) {
+    float total = s_acc[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    if (threadIdx.x == 0) {
+      if (reduction == FLCE_REDUCTION_MEAN) {
+        const int nv = *n_valid;
+        loss[0] = nv > 0 ? total / static_cast<float>(nv) : __int_as_float(0x7fc00000);
+      } else {
+        loss[0] = total;
+      }
     }
   }
 }
