@@ -77,7 +77,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int6
 // ---------------------------------------------------------------- layouts
 struct FlceLayout {
   int64_t chunk, num_chunks, vp, nvt;  // nvt: 256-column vocabulary tiles
-  int64_t npart;                       // room for per-row LSE partials: one per kPartColsMin columns
+  int64_t npart;                       // per-row LSE partials: one per part_cols(forward_epi_warps) columns
   int gh_slices;  // most K slices of a split grad_H (1: never split)
   size_t header, zbuf, partials, tgt_logit, row_lse, row_scale, row_tgt, loss_rows, gh_part, total;
   size_t cvt_h, cvt_w, cvt_b;  // fp32 operands: their bf16 copies (0 bytes otherwise)
@@ -115,7 +115,6 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   L->num_chunks = N > 0 ? ceil_div(N, L->chunk) : 0;
   L->vp = round_up(static_cast<size_t>(V), 8);
   L->nvt = ceil_div(V, kBN);
-  L->npart = ceil_div(V, kPartColsMin);
   size_t off = 0;
   L->header = off;
   off = round_up(off + sizeof(WorkspaceHeader) + sizeof(unsigned int) * 2 * (L->num_chunks + 1), kAlign);
@@ -125,6 +124,8 @@ bool flce_layout(int64_t N, int64_t H, int64_t V, int64_t chunk, int reduction, 
   const bool split = dtype == FLCE_DTYPE_FP32;
   const bool rounded = dtype == FLCE_DTYPE_FP32_ROUNDED;
   const size_t planes = split ? 2 : 1;
+  // LSE partials per row: one per column range of a forward epilogue warp
+  L->npart = ceil_div(V, part_cols(forward_epi_warps(H, split ? 3 : 1)));
   L->zbuf = off;
   L->z_plane = split ? L->chunk * static_cast<int64_t>(L->vp) : 0;
   off = round_up(off + planes * static_cast<size_t>(L->chunk) * L->vp * 2, kAlign);
@@ -369,7 +370,7 @@ flce_status_t flce_fwd_bwd_typed(int dtype, const void* hidden, const void* weig
     g.ldz = L.vp;
     g.partials = partials;
     g.epi_warps = forward_epi_warps(H, g.nseg);
-    g.nvt = static_cast<int>(ceil_div(V, part_cols(g.epi_warps)));
+    g.nvt = static_cast<int>(L.npart);  // the layout sized them for this warp count
     g.tgt_logit = tgt_logit;
     g.grad_hidden = fp32 ? nullptr : static_cast<uint16_t*>(grad_hidden);
     g.grad_hidden_f32 = fp32 ? static_cast<float*>(grad_hidden) : nullptr;
@@ -599,7 +600,7 @@ flce_status_t flce_vp_forward(const void* hidden, const void* weight_shard, cons
   g.ldz = L.vp;
   g.partials = reinterpret_cast<float4*>(ws + L.partials);
   g.epi_warps = forward_epi_warps(H, 1);
-  g.nvt = static_cast<int>(ceil_div(V_shard, part_cols(g.epi_warps)));
+  g.nvt = static_cast<int>(L.npart);
   g.tgt_logit = reinterpret_cast<float*>(ws + L.tgt_logit);
   g.status = status;
   g.timeout_ns = g_timeout_ns.load();

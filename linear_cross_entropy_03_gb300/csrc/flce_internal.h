@@ -15,10 +15,9 @@ constexpr int kBN = 256;          // tile columns (fp32 accumulator columns)
 constexpr int kBK = 64;           // k per pipeline stage (128 bytes of bf16)
 // Warps that drain the accumulators: 4 (one per TMEM lane quarter) or 8 (two
 // per quarter, each taking half of a tile's columns), chosen per launch.
-constexpr int kEpiWarpsMax = 8;
-// columns of a tile one epilogue warp drains, and so of one LSE partial
+// part_cols: columns of a tile one epilogue warp drains, and so of one LSE
+// partial (256 or 128).
 constexpr int part_cols(int epi_warps) { return kBN / (epi_warps / 4); }
-constexpr int kPartColsMin = part_cols(kEpiWarpsMax);  // 128
 // Forward launches use 8 epilogue warps when the k loop is short (H * nseg
 // below 4096), where draining a tile takes longer than its MMAs.
 inline int forward_epi_warps(int64_t H, int nseg) { return H * (nseg > 1 ? nseg : 1) < 4096 ? 8 : 4; }
