@@ -806,8 +806,19 @@ __global__ void __launch_bounds__(kRingThreads, 1) ce_rows_ring_kernel(const CeP
   // this group's rows: j = grp, grp + 2, ...; a row's scalars are loaded
   // before its data is waited for
   int iter = 0;
+  int b = grp, use = 0;  // j % depth and j / depth, kept up to date without divisions
+  while (b >= depth) {
+    b -= depth;
+    ++use;
+  }
   for (int j = grp; j < mine; j += kRingGroups, ++iter) {
-    const int b = j % depth, use = j / depth;
+    if (j != grp) {
+      b += kRingGroups;
+      while (b >= depth) {
+        b -= depth;
+        ++use;
+      }
+    }
     const int row = blockIdx.x + j * stride;
     const int64_t t = __ldg(p.target + row);
     const float go = p.grad_out != nullptr ? __ldg(p.grad_out + row) : 1.f;
