@@ -38,7 +38,13 @@ constexpr int kNarrowStageBytes = 2 * kHalf * kBK * 2;
 constexpr int kWideStages = 4;
 constexpr int kWideStageBytes = 3 * kHalf * kBK * 2;
 static_assert(kWideStages * kWideStageBytes <= kRingSlots * kNarrowStageBytes, "wide layout exceeds the ring");
-constexpr int kGemm2SmemBytes = kRingSlots * kNarrowStageBytes + 1024 + 1024;
+// Per CTA, 16 KB of staging for the epilogue's coalesced stores: 2 KB per
+// warp with 8 epilogue warps, 4 KB with 4 (store_rows16 / store_rows32f).
+constexpr int kEpiStageBytes = 16384;
+static_assert(kEpiStageBytes / 4 >= 32 * 32 * 4, "backward launches (4 epilogue warps) stage 32 x 32 fp32 per warp");
+static_assert(kEpiStageBytes / 8 >= 32 * 32 * 2, "8-warp forward launches stage 32 x 32 16-bit values per warp");
+// ring, barrier area (1 KB), epilogue staging, 1 KB of alignment slack
+constexpr int kGemm2SmemBytes = kRingSlots * kNarrowStageBytes + 1024 + kEpiStageBytes + 1024;
 // tile-ring consumers: leader MMA issuer + epilogue warps, peer producer + epilogue warps
 constexpr int ring_consumers(int epi_warps) { return 1 + epi_warps + 1 + epi_warps; }
 constexpr int gemm_threads(int epi_warps) { return 64 + 32 * epi_warps; }
@@ -152,6 +158,55 @@ __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias,
   }
 }
 
+// The epilogue holds one accumulator row per lane; stored as it is, every
+// warp store would write 32 rows 16 bytes each.  These two store a warp's 32
+// rows x 32 columns through its staging buffer instead: each lane writes its
+// row's 16-byte pieces, then reads back pieces of other rows so that each
+// store instruction covers whole 64- or 128-byte row segments.  The pieces'
+// slots are XOR-swizzled so that both the row-wise writes and the
+// column-wise reads touch eight different 16-byte bank groups per phase.
+//
+// 16-bit values (pk[i]: columns 2i, 2i + 1 of the lane's row); row r of the
+// 32 goes to row0 + r * ld; rows >= nrows and columns >= lim are skipped.
+__device__ __forceinline__ void store_rows16(uint4* stage, const uint32_t (&pk)[16], uint16_t* row0, int64_t ld,
+                                             int nrows, int c, int lim, int lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    stage[lane * 4 + (k ^ ((lane >> 1) & 3))] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+  __syncwarp();
+  const int k = lane & 3;  // this lane's 16-byte piece: columns 8k .. 8k + 7
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = (lane >> 2) + 8 * j;
+    const uint4 val = stage[r * 4 + (k ^ ((r >> 1) & 3))];
+    if (r < nrows && 8 * k < lim) __stcs(reinterpret_cast<uint4*>(row0 + r * ld + c + 8 * k), val);
+  }
+  __syncwarp();  // the buffer is rewritten by the next chunk
+}
+
+// fp32 values (a[k]: columns 4k .. 4k + 3 of the lane's row), stored or
+// added with vector reductions.
+__device__ __forceinline__ void store_rows32f(float4* stage, const float4 (&a)[8], float* row0, int64_t ld, int nrows,
+                                              int c, int lim, int lane, bool add) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) stage[lane * 8 + (k ^ (lane & 7))] = a[k];
+  __syncwarp();
+  const int k = lane & 7;  // this lane's 16-byte piece: columns 4k .. 4k + 3
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = (lane >> 3) + 4 * j;
+    const float4 val = stage[r * 8 + (k ^ (r & 7))];
+    if (r < nrows && 4 * k < lim) {
+      float4* dst = reinterpret_cast<float4*>(row0 + r * ld + c + 4 * k);
+      if (add)  // one fire-and-forget add per element and launch: the L2 does the read-add-write
+        red_add_f32x4(dst, val);
+      else
+        __stcs(dst, val);
+    }
+  }
+  __syncwarp();
+}
+
 // Epilogue of one tile for this warp's 32 accumulator rows (`rl` = row
 // within the pair tile of this thread) and its PC columns from c_lo (with 8
 // epilogue warps two share each TMEM lane quarter, one per half of the
@@ -162,17 +217,20 @@ __device__ __forceinline__ void add_bias32(float (&x)[32], const uint16_t* bias,
 // products.
 template <bool F16, bool SPLIT, int PC>
 __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams& p, uint32_t tbase, int rl,
-                                              int c_lo, float out_scale, int64_t row_target) {
+                                              int c_lo, float out_scale, int64_t row_target, uint8_t* stage) {
+  const int lane = threadIdx.x & 31;
+  const int wrow = rl - lane;  // the warp's first row within the pair tile
   if (ti.kind == 0) {
     const int r = ti.m0 + rl;
     const bool row_ok = r < p.c_len;
+    const int nrows = min(32, p.c_len - (ti.m0 + wrow));  // valid rows of the warp's 32
+    uint16_t* zrow0 = p.zbuf + static_cast<int64_t>(ti.m0 + wrow) * p.ldz + ti.n0;
     const int ncols = min(kBN, p.V - ti.n0);
     int t_rel = -1;
     if (row_ok) {
       const int64_t tg = row_target - p.v_offset;
       if (tg >= ti.n0 && tg < ti.n0 + ncols) t_rel = static_cast<int>(tg - ti.n0);
     }
-    uint16_t* zrow = p.zbuf + static_cast<int64_t>(row_ok ? r : 0) * p.ldz + ti.n0;
     float m_run = -INFINITY, s32 = 0.f, s16 = 0.f;
     for (int c = c_lo; c < c_lo + PC; c += 32) {
       if (c >= ncols) break;
@@ -252,23 +310,13 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
           if (j == t_rel - c) zt = x[j];
         p.tgt_logit[r] = zt;
       }
-      if (row_ok) {
+      store_rows16(reinterpret_cast<uint4*>(stage), pk, zrow0, p.ldz, nrows, c, lim, lane);
+      if (SPLIT) {  // the lower halves of the fp32 bits, one plane further
+        uint32_t lo[16];
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4)
-          if (8 * g4 < lim)
-            __stcs(reinterpret_cast<uint4*>(zrow + c + 8 * g4),
-                   make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]));
-        if (SPLIT) {  // the lower halves of the fp32 bits, one plane further
-          uint32_t lo[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            lo[i] = __byte_perm(__float_as_uint(x[2 * i]), __float_as_uint(x[2 * i + 1]), 0x5410);
-#pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4)
-            if (8 * g4 < lim)
-              __stcs(reinterpret_cast<uint4*>(zrow + p.z_plane + c + 8 * g4),
-                     make_uint4(lo[4 * g4], lo[4 * g4 + 1], lo[4 * g4 + 2], lo[4 * g4 + 3]));
-        }
+        for (int i = 0; i < 16; ++i)
+          lo[i] = __byte_perm(__float_as_uint(x[2 * i]), __float_as_uint(x[2 * i + 1]), 0x5410);
+        store_rows16(reinterpret_cast<uint4*>(stage), lo, zrow0 + p.z_plane, p.ldz, nrows, c, lim, lane);
       }
     }
     if (SPLIT) s16 = s32;  // the gradient is formed from the exact fp32 logits
@@ -317,30 +365,20 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
       }
     }
   } else {
-    const int vrow = ti.m0 + rl;
-    const bool row_ok = vrow < p.V;
+    const int nrows = min(32, p.V - (ti.m0 + wrow));  // valid vocabulary rows of the warp's 32
     const int ncols = min(kBN, p.H - ti.n0);
-    float* out = p.grad_weight + static_cast<int64_t>(row_ok ? vrow : 0) * p.H + ti.n0;
+    float* out0 = p.grad_weight + static_cast<int64_t>(ti.m0 + wrow) * p.H + ti.n0;
     for (int c = c_lo; c < c_lo + PC; c += 32) {
       if (c >= ncols) break;
       uint32_t v[32];
       tmem_load_32cols(tbase + c, v);
       tmem_load_wait();
-      if (row_ok) {
-        float4* o4 = reinterpret_cast<float4*>(out + c);
+      float4 a[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          if (c + 4 * g < ncols) {
-            const float4 a = make_float4(out_scale * __uint_as_float(v[4 * g]), out_scale * __uint_as_float(v[4 * g + 1]),
-                                         out_scale * __uint_as_float(v[4 * g + 2]),
-                                         out_scale * __uint_as_float(v[4 * g + 3]));
-            if (p.gw_store)
-              __stcs(o4 + g, a);
-            else  // one fire-and-forget add per element and launch: the L2 does the read-add-write
-              red_add_f32x4(o4 + g, a);
-          }
-        }
-      }
+      for (int g = 0; g < 8; ++g)
+        a[g] = make_float4(out_scale * __uint_as_float(v[4 * g]), out_scale * __uint_as_float(v[4 * g + 1]),
+                           out_scale * __uint_as_float(v[4 * g + 2]), out_scale * __uint_as_float(v[4 * g + 3]));
+      store_rows32f(reinterpret_cast<float4*>(stage), a, out0, p.H, nrows, c, ncols - c, lane, !p.gw_store);
     }
   }
 }
@@ -603,6 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
     const int q = warp & 3;                                // TMEM lane quarter (hardware rule: warp % 4)
     constexpr int PC = part_cols(EW);
     const int c_lo = ((warp - 2) / 4) * PC;               // this warp's columns of every tile
+    uint8_t* stage = bar_area + 1024 + (warp - 2) * (kEpiStageBytes / EW);  // this warp's staging buffer
     // fp16: the chunk's dZ was stored divided by the rows' common scale
     const float out_scale = (MODE == kModeBackward && p.in_fp16)
                                 ? uniform_scale(p.reduction, p.grad_scale, p.n_valid, p.gmax)
@@ -638,11 +677,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
         if (p.in_fp16)
-          epilogue_tile<true, false, PC>(ti, p, tbase, rl, c_lo, out_scale, row_target);
+          epilogue_tile<true, false, PC>(ti, p, tbase, rl, c_lo, out_scale, row_target, stage);
         else if (p.nseg > 1)
-          epilogue_tile<false, true, PC>(ti, p, tbase, rl, c_lo, 1.f, row_target);
+          epilogue_tile<false, true, PC>(ti, p, tbase, rl, c_lo, 1.f, row_target, stage);
         else
-          epilogue_tile<false, false, PC>(ti, p, tbase, rl, c_lo, 1.f, row_target);
+          epilogue_tile<false, false, PC>(ti, p, tbase, rl, c_lo, 1.f, row_target, stage);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(acc == 0 ? leader_tempty0 : leader_tempty1);
