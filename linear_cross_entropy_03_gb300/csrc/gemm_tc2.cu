@@ -184,10 +184,12 @@ __device__ __forceinline__ void store_rows16(uint4* stage, const uint32_t (&pk)[
   __syncwarp();  // the buffer is rewritten by the next chunk
 }
 
-// fp32 values (a[k]: columns 4k .. 4k + 3 of the lane's row), stored or
-// added with vector reductions.
+// fp32 values (a[k]: columns 4k .. 4k + 3 of the lane's row): streamed to
+// memory (kStoreStream), added with vector reductions (kStoreAdd), or
+// stored to stay in L2 for a kernel that reads them next (kStoreKeep).
+constexpr int kStoreStream = 0, kStoreAdd = 1, kStoreKeep = 2;
 __device__ __forceinline__ void store_rows32f(float4* stage, const float4 (&a)[8], float* row0, int64_t ld, int nrows,
-                                              int c, int lim, int lane, bool add) {
+                                              int c, int lim, int lane, int mode) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) stage[lane * 8 + (k ^ (lane & 7))] = a[k];
   __syncwarp();
@@ -198,8 +200,10 @@ __device__ __forceinline__ void store_rows32f(float4* stage, const float4 (&a)[8
     const float4 val = stage[r * 8 + (k ^ (r & 7))];
     if (r < nrows && 4 * k < lim) {
       float4* dst = reinterpret_cast<float4*>(row0 + r * ld + c + 4 * k);
-      if (add)  // one fire-and-forget add per element and launch: the L2 does the read-add-write
+      if (mode == kStoreAdd)  // one fire-and-forget add per element and launch: the L2 does the read-add-write
         red_add_f32x4(dst, val);
+      else if (mode == kStoreKeep)
+        __stcg(dst, val);
       else
         __stcs(dst, val);
     }
@@ -323,45 +327,33 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
     if (row_ok && ti.n0 + c_lo < p.V)
       p.partials[static_cast<int64_t>(r) * p.nvt + (ti.n0 + c_lo) / PC] = make_float4(m_run, s32, s16, 0.f);
   } else if (ti.kind == 1) {
-    const int r = ti.m0 + rl;
-    const bool row_ok = r < p.c_len;
+    const int nrows = min(32, p.c_len - (ti.m0 + wrow));  // valid rows of the warp's 32
     const int ncols = min(kBN, p.H - ti.n0);
-    const int64_t off = (p.row0 + (row_ok ? r : 0)) * static_cast<int64_t>(p.H) + ti.n0;
-    uint16_t* out = p.grad_hidden + off;
+    const int64_t row0 = ti.m0 + wrow;
+    const int64_t off = (p.row0 + row0) * static_cast<int64_t>(p.H) + ti.n0;
     // a K slice of a split tile: its fp32 partial sums, scaled like the output
-    float* part = p.h_split > 1 ? p.gh_part + ti.slice * p.gh_part_ld +
-                                      static_cast<int64_t>(row_ok ? r : 0) * p.H + ti.n0
-                                : nullptr;
+    float* part0 = p.h_split > 1 ? p.gh_part + ti.slice * p.gh_part_ld + row0 * p.H + ti.n0 : nullptr;
     for (int c = c_lo; c < c_lo + PC; c += 32) {
       if (c >= ncols) break;
       uint32_t v[32];
       tmem_load_32cols(tbase + c, v);
       tmem_load_wait();
-      if (row_ok && part != nullptr) {
-        float4* o4 = reinterpret_cast<float4*>(part + c);
+      if (part0 != nullptr || p.grad_hidden_f32 != nullptr) {
+        // fp32: a K slice's partial sums, or the fp32 output (fp32 operands, a shard's partial)
+        const float sc = part0 != nullptr ? out_scale : 1.f;
+        float4 a[8];
 #pragma unroll
         for (int g4 = 0; g4 < 8; ++g4)
-          if (c + 4 * g4 < ncols)
-            __stcg(o4 + g4, make_float4(out_scale * __uint_as_float(v[4 * g4]), out_scale * __uint_as_float(v[4 * g4 + 1]),
-                                        out_scale * __uint_as_float(v[4 * g4 + 2]),
-                                        out_scale * __uint_as_float(v[4 * g4 + 3])));
-      } else if (row_ok && p.grad_hidden_f32 != nullptr) {  // fp32 output (fp32 operands, a shard's partial)
-        float4* o4 = reinterpret_cast<float4*>(p.grad_hidden_f32 + off + c);
+          a[g4] = make_float4(sc * __uint_as_float(v[4 * g4]), sc * __uint_as_float(v[4 * g4 + 1]),
+                              sc * __uint_as_float(v[4 * g4 + 2]), sc * __uint_as_float(v[4 * g4 + 3]));
+        store_rows32f(reinterpret_cast<float4*>(stage), a, part0 != nullptr ? part0 : p.grad_hidden_f32 + off, p.H,
+                      nrows, c, ncols - c, lane, kStoreKeep);
+      } else {
+        uint32_t pk[16];
 #pragma unroll
-        for (int g4 = 0; g4 < 8; ++g4)
-          if (c + 4 * g4 < ncols)
-            o4[g4] = make_float4(__uint_as_float(v[4 * g4]), __uint_as_float(v[4 * g4 + 1]),
-                                 __uint_as_float(v[4 * g4 + 2]), __uint_as_float(v[4 * g4 + 3]));
-      } else if (row_ok) {
-        const int lim = ncols - c;
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4)
-          if (8 * g4 < lim)
-            *reinterpret_cast<uint4*>(out + c + 8 * g4) = make_uint4(
-                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 0]), out_scale * __uint_as_float(v[8 * g4 + 1])),
-                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 2]), out_scale * __uint_as_float(v[8 * g4 + 3])),
-                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 4]), out_scale * __uint_as_float(v[8 * g4 + 5])),
-                pack16<F16>(out_scale * __uint_as_float(v[8 * g4 + 6]), out_scale * __uint_as_float(v[8 * g4 + 7])));
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack16<F16>(out_scale * __uint_as_float(v[2 * i]), out_scale * __uint_as_float(v[2 * i + 1]));
+        store_rows16(reinterpret_cast<uint4*>(stage), pk, p.grad_hidden + off, p.H, nrows, c, ncols - c, lane);
       }
     }
   } else {
@@ -378,7 +370,8 @@ __device__ __forceinline__ void epilogue_tile(const Tile2& ti, const GemmParams&
       for (int g = 0; g < 8; ++g)
         a[g] = make_float4(out_scale * __uint_as_float(v[4 * g]), out_scale * __uint_as_float(v[4 * g + 1]),
                            out_scale * __uint_as_float(v[4 * g + 2]), out_scale * __uint_as_float(v[4 * g + 3]));
-      store_rows32f(reinterpret_cast<float4*>(stage), a, out0, p.H, nrows, c, ncols - c, lane, !p.gw_store);
+      store_rows32f(reinterpret_cast<float4*>(stage), a, out0, p.H, nrows, c, ncols - c, lane,
+                    p.gw_store ? kStoreStream : kStoreAdd);
     }
   }
 }
