@@ -55,12 +55,19 @@ KERNEL_SOURCES = [os.path.join(ROOT, "linear_cross_entropy_03_gb300", "csrc", f)
 
 
 def kernel_source_hash():
-    """First 16 hex digits of the sha256 over the backward GEMM's source files."""
+    """First 16 hex digits of the sha256 over the backward GEMM's source files,
+    comments and blank lines left out (an edit of a comment does not change
+    the kernel)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

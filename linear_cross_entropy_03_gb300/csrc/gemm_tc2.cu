@@ -16,7 +16,9 @@
 //             also the tile scheduler, which writes every tile id into both
 //             CTAs' rings
 //   warp 1    TMEM allocation for the pair; in the leader, the MMA issuer
-//   warps 2-5 epilogue of this CTA's 128 accumulator rows
+//   warps 2.. epilogue of this CTA's 128 accumulator rows: 4 warps (one per
+//             TMEM lane quarter), or 8 (two per quarter, each half of the
+//             columns) in forward launches with a short k loop
 // Operand bytes of both CTAs complete on the leader's stage barriers; the
 // leader's tcgen05.commit arrives on the matching barriers of both CTAs.
 #include <cuda_fp16.h>
