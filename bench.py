@@ -16,7 +16,13 @@ Printed as one JSON line (rank 0):
              the library during the timed region) against the measured bf16
              tensor peak;
   ce_on_logits  GB/s of ce_fwd_bwd (one read + one write of the logits) with
-             L2 flushed between calls, against the measured HBM copy peak;
+             L2 flushed between calls, against the measured HBM copy peak
+             (and the oracle's cross entropy on the same logits under
+             `oracle`);
+  workloads  one line per configuration of the method (tiny, the H = 128
+             shard, Llama-3.2-1B chunk sizes, the Llama-3-8B chunk sweep,
+             the 256k-vocabulary stress shape), each with the oracle timed
+             beside it;
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload.
 
 `--impl reference` times the oracle itself as the reference arm.
@@ -755,6 +761,21 @@ def oracle_sample(inp, rows: int):
     return time.perf_counter() - t0
 
 
+def ce_oracle_baseline():
+    """The fp64 oracle's cross entropy on the CE leg's whole problem (bf16
+    logits [1024, 32768], loss and gradient), timed on the host cores."""
+    from oracle import flce_oracle as O
+    import synthetic_inputs as si
+    n, v = CE_WORKLOAD["n"], CE_WORKLOAD["v"]
+    logits, tgt = si.make_ce_logits(n, v, si.CE_CONFIG["seed"])
+    t0 = time.perf_counter()
+    O.ce_reference(logits, tgt, reduction="mean")
+    secs = time.perf_counter() - t0
+    nbytes = 2 * n * v * 2 + 12 * n
+    return {"gbs": round(nbytes / secs / 1e9, 3), "secs": round(secs, 3), "cores": cores_used(), "kind": "oracle",
+            "sample": f"whole problem: fp64 numpy cross entropy, loss and gradient of bf16 logits [{n}, {v}]"}
+
+
 def cpu_baseline(inp, rows=512):
     secs = oracle_sample(inp, rows)
     return {"value": rows / secs, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
@@ -959,8 +980,11 @@ def main():
         workloads = every_workload(flce, device, step.stream, peaks, oracle=not args.no_cpu_baseline)
 
     cpu = None
+    ce_oracle = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, args.cpu_rows)
+        if not args.only_flce:
+            ce_oracle = ce_oracle_baseline()
 
     if rank == 0:
         line = {
@@ -986,7 +1010,8 @@ def main():
                                                  "what": "torch device-to-device copy of the 64 MB logits "
                                                          "into another buffer, timed the same way"},
                              "l2": "emptied before every call (256 MB written, then 256 MB read)", "scope": "gbs/frac: whole ce_fwd_bwd call "
-                             "(count + ce_rows kernels); kernel_*: ce_rows alone", "clocks": ce_clocks},
+                             "(count + ce_rows kernels); kernel_*: ce_rows alone", "clocks": ce_clocks,
+                             "oracle": ce_oracle},
             "scratch": {"workspace_bytes": step.ws_bytes, "peak_allocated_delta_bytes": peak_delta,
                         "full_logits_bytes": n * v * 2, "chunk": chunk, "chunks": n_chunks},
             "next_rows": widened,
