@@ -356,32 +356,93 @@ __global__ void __launch_bounds__(256)
 
 // The same with 16-byte vectors (rows of a multiple of 16 bytes, 16-byte
 // aligned): one vector per thread and step, grid (vectors of a row, rows).
+// Packed fp32x2 arithmetic: exp(z - lse) as ex2 of one fused multiply-add,
+// times the row scale; the target element's onehot is taken off in the one
+// vector that holds it.
+__device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8], uint16_t) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    x[2 * q] = bf16_lo(w[q]);
+    x[2 * q + 1] = bf16_hi(w[q]);
+  }
+}
+__device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8], __half) {
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __half22float2(h[q]);
+    x[2 * q] = f.x;
+    x[2 * q + 1] = f.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8], uint16_t) {
+  return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                    pack_bf16x2(x[6], x[7]));
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8], __half) {
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2 h = __floats2half2_rn(x[2 * q], x[2 * q + 1]);
+    w[q] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     ce_vp_grad_vec_kernel(const T* __restrict__ logits, T* grad, const int64_t* __restrict__ target, int64_t N,
                           int64_t V, int64_t v_offset, int64_t ignore_index, const float* __restrict__ lse,
                           const float* __restrict__ row_scale) {
   constexpr int EPV = 16 / sizeof(T);
+  constexpr float kL2e = 1.4426950408889634f;
   const int64_t nvec = V / EPV;
   for (int64_t row = blockIdx.y; row < N; row += gridDim.y) {
     const int64_t tg = target[row];
     const int64_t tl = tg - v_offset;
     const int64_t t = (tg != ignore_index && tl >= 0 && tl < V) ? tl : -1;
+    const int64_t tvec = t >= 0 ? t / EPV : -1;  // the vector holding the target, and its element
+    const int tel = t >= 0 ? static_cast<int>(t % EPV) : 0;
     const float sc = row_scale[row];
-    const float l = lse[row];
+    const float nl = -lse[row] * kL2e;
     const uint4* x = reinterpret_cast<const uint4*>(logits + row * V);
     uint4* g = reinterpret_cast<uint4*>(grad + row * V);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-      uint4 u = sc == 0.f ? make_uint4(0, 0, 0, 0) : __ldcs(x + i);
-      T* e = reinterpret_cast<T*>(&u);
-#pragma unroll
-      for (int k = 0; k < EPV; ++k) {
-        const int64_t v = i * EPV + k;
-        const float d = sc == 0.f ? 0.f : sc * (__expf(load_as_f(e + k) - l) - (v == t ? 1.f : 0.f));
-        store_f(e + k, d);
+      if (sc == 0.f) {  // an ignored row (or grad_out 0): zero gradient
+        __stcs(g + i, make_uint4(0, 0, 0, 0));
+        continue;
       }
-      __stcs(g + i, u);
+      const uint4 u = __ldcs(x + i);
+      float z[8];
+      if constexpr (EPV == 8) {
+        unpack8(u, z, T());
+      } else {
+        z[0] = __uint_as_float(u.x);
+        z[1] = __uint_as_float(u.y);
+        z[2] = __uint_as_float(u.z);
+        z[3] = __uint_as_float(u.w);
+      }
+      const float2 l2e = make_float2(kL2e, kL2e), nl2 = make_float2(nl, nl), sc2 = make_float2(sc, sc);
+#pragma unroll
+      for (int q = 0; q < EPV / 2; ++q) {
+        const float2 a = __ffma2_rn(make_float2(z[2 * q], z[2 * q + 1]), l2e, nl2);
+        const float2 d = __fmul2_rn(make_float2(ex2_approx(a.x), ex2_approx(a.y)), sc2);
+        z[2 * q] = d.x;
+        z[2 * q + 1] = d.y;
+      }
+      if (i == tvec) {
+#pragma unroll
+        for (int k = 0; k < EPV; ++k)
+          if (k == tel) z[k] -= sc;
+      }
+      if constexpr (EPV == 8) {
+        __stcs(g + i, pack8(z, T()));
+      } else {
+        __stcs(g + i, make_uint4(__float_as_uint(z[0]), __float_as_uint(z[1]), __float_as_uint(z[2]),
+                                 __float_as_uint(z[3])));
+      }
     }
   }
 }
