@@ -720,6 +720,11 @@ flce_status_t ce_vp_partials(const void* logits, int dtype, const int64_t* targe
   if (N == 0) return FLCE_OK;
   const bool ptrs16 = aligned(logits, 16);
   const bool vec = (static_cast<size_t>(V_shard) * esz) % 16 == 0 && ptrs16;
+  if (vp_partials_rows_fits(dtype, V_shard, vec)) {
+    FLCE_TRY_CUDA(launch_vp_partials_rows(logits, dtype, target, N, V_shard, vocab_offset, ignore_index, lse_shard,
+                                          target_logit_shard, stream));
+    return FLCE_OK;
+  }
   const int64_t cap = ce_cta_capacity(dtype, vec);
   const int64_t epv = ce_vector_elems(dtype, vec);
   int64_t cl = ceil_div(V_shard, cap);

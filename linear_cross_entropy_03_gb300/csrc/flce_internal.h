@@ -224,6 +224,10 @@ cudaError_t launch_gh_reduce(const float* part, int slices, int64_t ld, int rows
                              uint16_t* out16, int f16, float* out32, cudaStream_t s);
 // vector_path: rows are whole 16-byte vectors and both pointers 16-byte
 // aligned; aligned_ptrs: both pointers 16-byte aligned (rows of any length).
+bool vp_partials_rows_fits(int dtype, int64_t V, bool vector_path);
+cudaError_t launch_vp_partials_rows(const void* logits, int dtype, const int64_t* target, int64_t N, int64_t V,
+                                    int64_t v_offset, int64_t ignore_index, float* lse_out, float* zt_out,
+                                    cudaStream_t s);
 cudaError_t launch_ce_rows(const CeParams& p, int dtype, bool vector_path, bool aligned_ptrs, bool pdl,
                            cudaStream_t s);
 // Whether rows of V elements go to a form that supports the single launch
