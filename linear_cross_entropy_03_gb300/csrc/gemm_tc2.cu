@@ -497,7 +497,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
           const uint32_t sa = base + stage * sbytes;
           const uint32_t sb = sa + kHalf * kBK * 2;
           const uint32_t fb = map_to_cta(smem_addr(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(smem_addr(&full[stage]), ti.kind == 1 ? 6 * kBoxBytes * 2 : 4 * kBoxBytes * 2);
+          // a wide grad_H tile whose second half lies wholly past H (H <= 256)
+          // loads and multiplies its first half only
+          const bool half1 = ti.kind == 1 && ti.n0 + kBN < p.H;
+          if (leader)
+            mbar_arrive_expect_tx(smem_addr(&full[stage]), (half1 ? 6 : 4) * kBoxBytes * 2);
           // k block kb: with split fp32 operands the three segments
           // (hi.hi, hi.lo, lo.hi) of each 64-wide k slice follow one another,
           // so the hi tile a segment re-reads is still in L2
@@ -524,8 +528,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
             tma_load_2d_pair(sa + kBoxBytes, m_z, fb, k0, mh + 64);
             tma_load_2d_pair(sb, m_w, fb, nh, k0);
             tma_load_2d_pair(sb + kBoxBytes, m_w, fb, nh + 64, k0);
-            tma_load_2d_pair(sb + 2 * kBoxBytes, m_w, fb, nh + kBN, k0);
-            tma_load_2d_pair(sb + 3 * kBoxBytes, m_w, fb, nh + kBN + 64, k0);
+            if (half1) {
+              tma_load_2d_pair(sb + 2 * kBoxBytes, m_w, fb, nh + kBN, k0);
+              tma_load_2d_pair(sb + 3 * kBoxBytes, m_w, fb, nh + kBN + 64, k0);
+            }
           } else {
             // grad_W: every tile re-reads the chunk's hidden rows (kept in L2);
             // each dZ column panel serves only the tiles of one vocabulary row
@@ -588,6 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
         const int nst = wide ? kWideStages : kRingSlots;
         const uint32_t sbytes = wide ? kWideStageBytes : kNarrowStageBytes;
         tc_fence_after_sync();
+        const bool half1 = ti.kind == 1 && ti.n0 + kBN < p.H;  // as the producer decides
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(bufs[0] * kBN);
         const uint32_t d_tmem1 = tmem_base + static_cast<uint32_t>(bufs[1] * kBN);
         uint32_t idesc = ti.kind == 0   ? instr_desc_bf16(256, kBN, 0, 0)
@@ -611,8 +618,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads(EW), 1)
                                              : smem_desc(sb + k * 2048, 8192, 1024);
             if (ti.kind == 1) {  // wide tile: the two 256-column halves share A
               mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-              mma_bf16_pair(
-                  d_tmem1, ad, smem_desc(sb + 2 * kBoxBytes + k * 2048, 8192, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
+              if (half1)  // (a second half wholly past H is neither loaded nor multiplied)
+                mma_bf16_pair(d_tmem1, ad, smem_desc(sb + 2 * kBoxBytes + k * 2048, 8192, 1024), idesc,
+                              (kb | k) != 0 ? 1u : 0u);
             } else {
               mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
